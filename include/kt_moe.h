@@ -1,0 +1,235 @@
+/*
+ * kt_moe.h -- C ABI of the GB300 (sm_103a) fused MXFP4-weight MoE layer.
+ *
+ * The layer (one mixture-of-experts block of a DeepSeek-V4-Flash- or
+ * Kimi-K3-shaped model) computes, for T tokens of hidden size H routed top-k
+ * over E experts of FC2 inter size I:
+ *
+ *   route:    topk_ids, topk_w = top-k of router logits, softmax weights
+ *   permute:  slots s = t*k + j grouped by expert (stable), expert offsets
+ *   quant:    A1 = MXFP8(hidden)            e4m3 + e8m0 per 32 along H
+ *   FC1:      G|U = A1 . w13[e]^T           w13 = gate rows | up rows (2I)
+ *   SwiGLU:   h = silu(G) * U;  A2 = MXFP8(h) (e8m0 per 32 along I)
+ *   FC2:      Y = A2 . w2[e]^T
+ *   combine:  out[t] = sum_j topk_w[t, j] * Y[slot t*k+j]
+ *
+ * Sources: "[MXFP4 layerwise prefill] SM 8.6 (Ampere) excluded by capability
+ * whitelist" (KTransformers issue 2172; Summary, Impact and Environment:
+ * native-MXFP4 DeepSeek-V4-Flash, 256 experts / top-6, 43 MoE layers, the
+ * per-layer "load experts -> compute -> sync" chain and the double-buffered
+ * layerwise prefill it wants instead) and "Kimi-K3 SM120 FlashInfer MXFP4
+ * MoE" (Goal: MXFP8 activation x MXFP4 weight fused MoE; on-device evidence:
+ * gated FC1 inter size = 2 x FC2 inter size; Phase 0 audit, item 4: SwiGLU
+ * gated layout).  Element formats follow the OCP MX v1.0 specification:
+ * MXFP4 = e2m1 elements, MXFP8 = e4m3 elements, one e8m0 scale per 32.
+ *
+ * Data formats at this boundary (all row-major, C order):
+ *   bf16       uint16_t bit patterns of bfloat16
+ *   fp4x2      uint8_t, two e2m1 values per byte: element 2i in bits 0-3,
+ *              element 2i+1 in bits 4-7
+ *   e8m0       uint8_t scale byte s meaning 2^(s-127); 255 (NaN) not allowed
+ *   e4m3       uint8_t OCP E4M3FN code
+ *
+ * Conventions for every entry point:
+ *   - All pointers are DEVICE pointers unless stated otherwise; the caller
+ *     owns every buffer.  `stream` is a cudaStream_t passed as void*
+ *     (NULL = the legacy default stream).
+ *   - Calls are asynchronous on `stream` and never synchronise the device
+ *     (except kt_moe_read_device_error, which reads one word back).
+ *   - Arguments are checked before anything is launched; a failed check
+ *     returns an error and launches nothing.
+ *   - The forward and routing calls allocate no device memory: scratch
+ *     lives in the caller's workspace `ws` (see kt_moe_workspace_bytes).
+ *   - A workspace may be reused by consecutive calls on one stream; calls
+ *     that share a workspace must not overlap on the GPU.
+ *   - Kernels are built for sm_103a only; other devices get KT_ERR_CUDA.
+ */
+#ifndef KT_MOE_H
+#define KT_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int kt_status;
+
+#define KT_OK 0
+#define KT_ERR_INVALID_ARG (-1)       /* null pointer, negative size, k out of range */
+#define KT_ERR_UNSUPPORTED_SHAPE (-2) /* H or I not a multiple of 128, E > 1024, k > 32, ... */
+#define KT_ERR_WORKSPACE (-3)         /* ws too small or not 256-byte aligned */
+#define KT_ERR_CUDA (-4)              /* a CUDA runtime/driver call or launch failed */
+#define KT_ERR_TIMEOUT (-5)           /* a host-side wait passed its deadline */
+#define KT_ERR_DEVICE_TIMEOUT (-6)    /* a kernel's bounded wait expired (device error word) */
+#define KT_ERR_ALIGNMENT (-7)         /* a pointer is not aligned as documented */
+#define KT_ERR_BAD_EXPERT_ID (-8)     /* device error word: a topk id was outside [0, E) */
+
+/* Bits of the device error word (kt_moe_read_device_error). */
+#define KT_DEVERR_BAD_EXPERT_ID 0x1   /* an id outside [0, E): that slot contributed 0 */
+#define KT_DEVERR_TIMEOUT_LOAD 0x2    /* GEMM producer wait expired */
+#define KT_DEVERR_TIMEOUT_MMA 0x4     /* GEMM MMA-issuer wait expired */
+#define KT_DEVERR_TIMEOUT_EPI 0x8     /* GEMM epilogue wait expired */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* kt_status_string(kt_status status);
+
+/* ------------------------------------------------------------------ */
+/* Routing + permutation (route and permute steps).                   */
+/* ------------------------------------------------------------------ */
+
+/* Workspace bytes kt_moe_route_permute needs for T tokens, E experts, top-k. */
+size_t kt_moe_route_workspace_bytes(int T, int E, int k);
+
+/*
+ * Top-k routing and the token-to-expert permutation.
+ *   logits         f32 [T, E]  router logits (finite)
+ *   renormalize    1: topk_w = softmax over the k selected logits
+ *                  0: topk_w = full softmax over E, taken at the selected experts
+ *   topk_ids       i32 [T, k]  out: experts by (logit desc, index asc)
+ *   topk_w         f32 [T, k]  out: gating weights (computed in fp64, rounded)
+ *   expert_offsets i32 [E+1]   out: exclusive prefix of per-expert slot counts
+ *   perm           i32 [T*k]   out: perm[p] = slot s = t*k+j of permuted row p,
+ *                              grouped by expert, stable in slot order
+ *   inv_perm       i32 [T*k]   out: inv_perm[s] = p
+ *   ws, ws_bytes   scratch, >= kt_moe_route_workspace_bytes(T, E, k), 256-B aligned
+ * Limits: 1 <= k <= min(E, 32), E <= 1024, T >= 0 (T == 0 is a no-op).
+ * Errors: KT_ERR_INVALID_ARG, KT_ERR_UNSUPPORTED_SHAPE, KT_ERR_WORKSPACE,
+ * KT_ERR_ALIGNMENT (pointers must be 4-byte aligned), KT_ERR_CUDA.
+ */
+kt_status kt_moe_route_permute(const float* logits, int T, int E, int k, int renormalize,
+                               int32_t* topk_ids, float* topk_w, int32_t* expert_offsets,
+                               int32_t* perm, int32_t* inv_perm,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ */
+/* The fused layer forward (quant, FC1 + SwiGLU + requant, FC2 +      */
+/* combine; it re-derives the permutation from topk_ids).             */
+/* ------------------------------------------------------------------ */
+
+/* Workspace bytes kt_mxfp4_moe_forward needs (0 if a size is invalid). */
+size_t kt_moe_workspace_bytes(int T, int H, int I, int E, int k);
+
+/*
+ * One MoE layer forward on one GPU.
+ *   hidden   bf16  [T, H]            activations
+ *   topk_ids i32   [T, k]            expert of each slot; ids outside [0, E)
+ *                                    are skipped (that slot adds 0) and set
+ *                                    KT_DEVERR_BAD_EXPERT_ID
+ *   topk_w   f32   [T, k]            gating weights
+ *   w13      fp4x2 [E, 2I, H/2]      FC1 weights: rows [0, I) gate, [I, 2I) up
+ *   w13_sf   e8m0  [E, 2I, H/32]
+ *   w2       fp4x2 [E, H, I/2]       FC2 weights
+ *   w2_sf    e8m0  [E, H, I/32]
+ *   out      bf16  [T, H]            result (written, not accumulated)
+ *   ws       >= kt_moe_workspace_bytes(T, H, I, E, k) bytes, 256-B aligned
+ * Shape limits: H % 128 == 0, I % 128 == 0, 1 <= k <= min(E, 32),
+ * E <= 1024, T >= 0 (T == 0 returns KT_OK and launches nothing).
+ * The gated FC1 has 2I rows per expert, twice the FC2 inter size I; the
+ * signature carries I once, so that relation holds by construction.
+ * Alignment: hidden/out/topk_*: 16 B; w13/w2: 32 B; w13_sf/w2_sf: 16 B.
+ * Errors: KT_ERR_INVALID_ARG, KT_ERR_UNSUPPORTED_SHAPE, KT_ERR_ALIGNMENT,
+ * KT_ERR_WORKSPACE, KT_ERR_CUDA.  Device-side conditions are reported
+ * through the error word (kt_moe_read_device_error), which every forward
+ * call clears first.
+ */
+kt_status kt_mxfp4_moe_forward(const uint16_t* hidden, int T, int H,
+                               const int32_t* topk_ids, const float* topk_w, int k,
+                               const uint8_t* w13, const uint8_t* w13_sf,
+                               const uint8_t* w2, const uint8_t* w2_sf, int E, int I,
+                               uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Byte offsets of the forward's intermediates inside its workspace, so that
+ * tests and tools can read them after a call (all relative to ws):
+ *   err            i32 device error word
+ *   expert_offsets i32 [E+1]      chunk_prefix i32 [E+1] (token chunks per expert)
+ *   perm, inv_perm i32 [S]        S = T*k
+ *   hist           i32 [tiles*E]  permutation scratch
+ *   a1 e4m3 [S, H], a1_sf e8m0 [S, H/32]   (rows in permuted order)
+ *   a2 e4m3 [S, I], a2_sf e8m0 [S, I/32]   (rows in permuted order)
+ *   y  bf16 [S, H]  topk_w-weighted FC2 output, rows in slot order
+ */
+typedef struct kt_ws_layout {
+    size_t err, expert_offsets, chunk_prefix, perm, inv_perm, hist;
+    size_t a1, a1_sf, a2, a2_sf, y;
+    size_t total;
+} kt_ws_layout;
+
+kt_status kt_moe_workspace_layout(int T, int H, int I, int E, int k, kt_ws_layout* layout);
+
+/*
+ * Copy the device error word of a forward (or routing) workspace to *code
+ * (host int).  Synchronises `stream` first; returns KT_OK, or
+ * KT_ERR_DEVICE_TIMEOUT / KT_ERR_BAD_EXPERT_ID when the word has those bits.
+ */
+kt_status kt_moe_read_device_error(const void* ws, int* code, void* stream);
+
+/*
+ * Diagnostic entry: the block-scaled grouped GEMM alone, fp32 out.
+ *   act     e4m3 [S, K] + act_sf e8m0 [S, K/32]  rows grouped by expert
+ *   expert_offsets i32 [E+1] (device)            row ranges per expert
+ *   w       fp4x2 [E, N, K/2] + w_sf e8m0 [E, N, K/32]
+ *   out     f32 [S, N]: out[p, n] = sum_K act[p] * w[e(p), n] (block-scaled);
+ *           rows outside [expert_offsets[0], expert_offsets[E]) untouched
+ *   ws      >= kt_mx_gemm_workspace_bytes(E) bytes
+ * Limits: K % 128 == 0, N % 128 == 0, E <= 1024.
+ */
+size_t kt_mx_gemm_workspace_bytes(int E);
+kt_status kt_mx_grouped_gemm_f32(const uint8_t* act, const uint8_t* act_sf, int S, int K,
+                                 const int32_t* expert_offsets,
+                                 const uint8_t* w, const uint8_t* w_sf, int E, int N,
+                                 float* out, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ */
+/* Layerwise prefill: stream layer l+1's experts host -> device while  */
+/* layer l computes (issue 2172, Background / motivation).             */
+/* ------------------------------------------------------------------ */
+
+typedef struct kt_layerwise kt_layerwise;
+
+/* Bytes of one layer's packed expert store: w13 | w13_sf | w2 | w2_sf,
+ * each region starting at a 256-byte multiple (offsets via
+ * kt_layerwise_pack_offsets). */
+size_t kt_layerwise_pack_bytes(int H, int I, int E);
+kt_status kt_layerwise_pack_offsets(int H, int I, int E, size_t* w13, size_t* w13_sf,
+                                    size_t* w2, size_t* w2_sf);
+
+/*
+ * Create a layerwise context for L layers.  host_packs[l] is a HOST pointer
+ * (pinned, e.g. cudaHostAlloc) to layer l's pack; the array is copied, the
+ * packs are not and must outlive the context.  The context allocates (and
+ * destroy frees) two device pack slots, the per-call workspace for up to
+ * T_max tokens, two ping-pong hidden buffers, routing buffers, one copy
+ * stream and its events.  Uses the current device.
+ */
+kt_status kt_layerwise_create(kt_layerwise** ctx, int L, int H, int I, int E, int k, int T_max,
+                              const void* const* host_packs);
+
+/*
+ * Run all L layers: h_0 = hidden, h_{l+1} = MoE_l(h_l), out = h_L.
+ *   hidden bf16 [T, H] (device), logits: HOST array of L device pointers,
+ *   each f32 [T, E]; out bf16 [T, H] (device); T <= T_max.
+ * serialized_control = 0: double-buffered streaming -- the copy stream
+ *   uploads layer l+1 into the other slot while `stream` computes layer l.
+ * serialized_control = 1: the per-layer "upload all experts -> compute ->
+ *   synchronise" chain, kept as the measurement control.
+ * Routing uses renormalized top-k softmax.  Returns after enqueueing all
+ * work (serialized_control = 1 also synchronises per layer); host waits are
+ * bounded and return KT_ERR_TIMEOUT.
+ */
+kt_status kt_layerwise_prefill(kt_layerwise* ctx, const uint16_t* hidden, const float* const* logits,
+                               uint16_t* out, int T, int serialized_control, void* stream);
+
+/* Test hook: make the copy step of layer `layer` report KT_ERR_CUDA
+ * (-1 disables).  The pipeline must drain both streams and return it. */
+kt_status kt_layerwise_inject_copy_failure(kt_layerwise* ctx, int layer);
+
+kt_status kt_layerwise_destroy(kt_layerwise* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KT_MOE_H */
