@@ -1,0 +1,395 @@
+#!/usr/bin/env python
+"""Benchmark of the fused MXFP4-weight MoE layer on GB300: tokens/s and the
+fraction of the block-scaled roofline.
+
+One step = one pass of the layer's hot path over one batch: top-k routing
+from router logits, permutation, MXFP8 activation quantisation, FC1 +
+SwiGLU + requant, FC2 + combine (``kt_moe_route_permute`` then
+``kt_mxfp4_moe_forward``).  Inputs are seeded and synthetic, resident in HBM
+when the timed region starts; ``e2e`` repeats the measurement with the
+step's inputs (hidden, logits) copied from pinned host memory and the output
+copied back inside the timed region.
+
+Default workload: the DeepSeek-V4-Flash-shaped layer (T=4096 tokens, H=4096,
+E=256 experts, top-6, I=2048, Zipf(1.1)-skewed router logits).  Its expert
+weights (3.3 GB) are far larger than L2, so every step streams them from HBM
+(no L2 flush is needed between steps).
+
+``--impl reference`` times the fp64 CPU oracle (the only reference
+implementation; the pages ship no code) on the host cores, on a bounded
+token sample per step, and prints the same JSON line with "impl":
+"reference".  Under torchrun (N > 1) every rank runs an independent replica
+(the layer does not shard on one GPU per box); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import mxfp4_weight_moe_gb300 as kt  # noqa: E402
+from mxfp4_weight_moe_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = "MXFP4 fused-MoE layer tokens/s at 1 GB300; % of block-scaled roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0     # nominal dense ratio (4.5 / 2.25 PFLOP/s); mxf8f6f4 runs at the fp8 rate
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            self.ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:  # noqa: BLE001
+            self.ident = str(device.index or 0)
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.ident, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+
+        sm = [num(r[1]) for r in rows]
+        mx = [num(r[2]) for r in rows]
+        power = [num(r[3]) for r in rows]
+        reasons = set()
+        for r in rows:
+            for name, col in (("hw_slowdown", 5), ("hw_thermal_slowdown", 6), ("sw_thermal_slowdown", 7),
+                              ("sw_power_cap", 8)):
+                if r[col].lower().startswith("active"):
+                    reasons.add(name)
+        loaded = [s for s, p in zip(sm, power) if p == p] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": max(p for p in power if p == p) if any(p == p for p in power)
+                else None}
+
+
+# ------------------------------------------------------------------ work accounting
+def algorithmic(cfg, touched: int):
+    """Algorithmic FLOPs and HBM bytes of one layer step and of each GEMM launch.
+
+    FLOPs = 6*H*I*S (FC1 4HI + FC2 2HI per slot).  Bytes = touched experts x
+    (w13 + w2 + their e8m0 scales = 1.59375*H*I) + bf16 hidden in and out
+    (4*T*H) + ids and weights (8*S); intermediates are implementation traffic."""
+    H, I, S, T = cfg.H, cfg.I, cfg.S, cfg.T
+    w13_bytes = 2 * I * H // 2 + 2 * I * H // 32
+    w2_bytes = H * I // 2 + H * I // 32
+    return {
+        "layer_flops": 6.0 * H * I * S,
+        "layer_bytes": float(touched * (w13_bytes + w2_bytes) + 4 * T * H + 8 * S),
+        "fc1_bytes": float(touched * w13_bytes), "fc1_flops": 4.0 * H * I * S,
+        "fc2_bytes": float(touched * w2_bytes), "fc2_flops": 2.0 * H * I * S,
+        "w13_bytes_per_expert": w13_bytes, "w2_bytes_per_expert": w2_bytes,
+    }
+
+
+def workload_desc(cfg):
+    return (f"{cfg.name}: T={cfg.T} H={cfg.H} E={cfg.E} top_k={cfg.k} I={cfg.I} "
+            f"logits={cfg.logits} seed={cfg.seed}")
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_tokens_per_s(cfg, hidden, ids_np, w_np, W_host, n_tokens, seed=0):
+    import oracle as O
+
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(cfg.T, size=min(n_tokens, cfg.T), replace=False)).astype(np.int32)
+    hb = hidden.cpu().view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    O.moe_forward(hb, ids_np, w_np, *W_host, tokens=toks, want=("out",))
+    dt = time.perf_counter() - t0
+    return len(toks) / dt, dt, len(toks)
+
+
+def cpu_baseline(cfg, hidden, logits, W, target_s=12.0):
+    import oracle as O
+
+    W_host = [t.cpu().numpy() for t in W]
+    lg = logits.cpu().numpy()
+    ids_np, w_np = O.route(lg, cfg.k)
+    rate, dt, n = oracle_tokens_per_s(cfg, hidden, ids_np, w_np, W_host, 16)
+    n2 = int(min(cfg.T, max(16, rate * target_s)))
+    rate, dt, n = oracle_tokens_per_s(cfg, hidden, ids_np, w_np, W_host, n2, seed=1)
+    return {"value": rate, "unit": "tokens/s", "cores": O.max_threads(), "kind": "oracle",
+            "sample": f"{n} of {cfg.T} tokens (seeded, all {cfg.k} experts each) through the fp64 oracle "
+                      f"forward ({dt:.1f} s); routing excluded"}
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args, cfg, world, rank):
+    if rank != 0:
+        return None
+    import oracle as O
+
+    dev = "cpu"
+    hidden = syn.make_hidden(cfg.T, cfg.H, cfg.seed, device=dev)
+    logits = syn.make_logits(cfg.T, cfg.E, cfg.logits, cfg.seed, device=dev)
+    W = syn.make_weights(cfg.E, cfg.H, cfg.I, seed=cfg.seed, device=dev)
+    W_host = [t.numpy() for t in W]
+    hb = hidden.view(torch.int16).numpy().view(np.uint16)
+    lg = logits.numpy()
+    # calibrate tokens per step so the whole run takes about `budget` seconds
+    budget = float(args.ref_budget_s)
+    t0 = time.perf_counter()
+    ids, w = O.route(lg[:8], cfg.k)
+    O.moe_forward(hb[:8], ids, w, *W_host, want=("out",))
+    per_tok = (time.perf_counter() - t0) / 8
+    n_per_step = int(max(1, min(cfg.T, budget / max(1, args.steps + args.warmup) / per_tok)))
+    rng = np.random.default_rng(0)
+
+    def step(i):
+        toks = np.sort(rng.choice(cfg.T, size=n_per_step, replace=False))
+        ids, w = O.route(lg[toks], cfg.k)
+        O.moe_forward(hb[toks], ids, w, *W_host, want=("out",))
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = n_per_step * args.steps / dt
+    sample = (f"{n_per_step} of {cfg.T} tokens per step (seeded), route + forward in fp64 on the host cores; "
+              f"{args.steps} steps in {dt:.1f} s")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "T": cfg.T, "H": cfg.H, "E": cfg.E, "top_k": cfg.k,
+                   "I": cfg.I, "parallelism": "replicas", "l2": "n/a (host)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": O.max_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_ours(args, cfg, world, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    hidden = syn.make_hidden(cfg.T, cfg.H, cfg.seed, device=dev)
+    logits = syn.make_logits(cfg.T, cfg.E, cfg.logits, cfg.seed, device=dev)
+    W = syn.make_weights(cfg.E, cfg.H, cfg.I, seed=cfg.seed, device=dev)
+    T, E, k, H, I = cfg.T, cfg.E, cfg.k, cfg.H, cfg.I
+    route_out = (torch.empty(T, k, dtype=torch.int32, device=dev), torch.empty(T, k, dtype=torch.float32, device=dev),
+                 torch.empty(E + 1, dtype=torch.int32, device=dev), torch.empty(T * k, dtype=torch.int32, device=dev),
+                 torch.empty(T * k, dtype=torch.int32, device=dev))
+    ws_route = torch.empty(int(kt.lib().kt_moe_route_workspace_bytes(T, E, k)), dtype=torch.uint8, device=dev)
+    ws = torch.empty(kt.workspace_bytes(T, H, I, E, k), dtype=torch.uint8, device=dev)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(h=hidden, lg=logits):
+        ids, w, *_ = kt.route_permute(lg, k, out=route_out, workspace=ws_route, stream=stream)
+        kt.forward(h, ids, w, *W, out=out, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert kt.read_device_error(ws) == 0, "device error word set during warm-up"
+    counts = (route_out[2][1:] - route_out[2][:-1]).cpu()
+    touched = int((counts > 0).sum())
+
+    # ---- timed region: device-resident inputs
+    sampler = ClockSampler(dev)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = kt.kernel_launches()
+    kt.profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    elapsed_ms = ev0.elapsed_time(ev1)
+    launches = kt.kernel_launches() - launches0
+    prof = kt.profile_read()
+    kt.profile_enable(False)
+    clocks = sampler.stop()
+    ms_per_step = max_over_ranks(elapsed_ms / args.steps, world, dev)
+    value = T * world / (ms_per_step / 1e3)
+
+    # ---- e2e: host buffers in, host buffer out, copies inside the timed region
+    h_host = hidden.cpu().pin_memory()
+    lg_host = logits.cpu().pin_memory()
+    out_host = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    h_dev = torch.empty_like(hidden)
+    lg_dev = torch.empty_like(logits)
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        h_dev.copy_(h_host, non_blocking=True)
+        lg_dev.copy_(lg_host, non_blocking=True)
+        step(h_dev, lg_dev)
+        out_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ev0.record(stream)
+    for _ in range(e2e_steps):
+        h_dev.copy_(h_host, non_blocking=True)
+        lg_dev.copy_(lg_host, non_blocking=True)
+        step(h_dev, lg_dev)
+        out_host.copy_(out, non_blocking=True)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e2e_steps, world, dev)
+    assert torch.equal(out_host.view(torch.int16), out.cpu().view(torch.int16))
+
+    # ---- roofline of the dominant kernel (FC1 grouped GEMM) and of the layer
+    work = algorithmic(cfg, touched)
+    fc1_ms = prof["fc1"][0] / max(1, prof["fc1"][1])
+    fc2_ms = prof["fc2"][0] / max(1, prof["fc2"][1])
+    hbm = float(peaks["hbm_gbs"])
+    mx_tflops = float(peaks["bf16_tflops"]) * FP8_OVER_BF16
+    fc1_gbs = work["fc1_bytes"] / (fc1_ms / 1e3) / 1e9
+    t_roof_ms = 1e3 * max(work["layer_flops"] / (mx_tflops * 1e12), work["layer_bytes"] / (hbm * 1e9))
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxfp8xmxfp4", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "T": T, "H": H, "E": E, "top_k": k, "I": I,
+                   "touched_experts": touched, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": f"inputs larger than L2 ({work['layer_bytes'] / 1e9:.2f} GB of weights+activations per step)"},
+        "e2e": {"value": T * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": hidden.numel() * 2 + logits.numel() * 4,
+                "d2h_bytes_per_step": out.numel() * 2},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "roofline": {"bound": "hbm", "achieved": fc1_gbs, "peak": hbm, "unit": "GB/s", "frac": fc1_gbs / hbm,
+                     "traffic": None, "kernel": "mx_gemm_kernel<SwiGLU> (FC1)",
+                     "peak_source": f"{peak_src} hbm_gbs",
+                     "algorithmic_bytes_per_launch": work["fc1_bytes"], "avg_launch_ms": fc1_ms},
+        "layer_roofline": {"t_roof_ms": t_roof_ms, "frac": t_roof_ms / ms_per_step,
+                           "bytes": work["layer_bytes"], "flops": work["layer_flops"],
+                           "hbm_gbs": hbm, "mx_tflops": mx_tflops,
+                           "peaks": f"{peak_src}: hbm_gbs; bf16_tflops x {FP8_OVER_BF16} (nominal fp8/bf16)"},
+        "stage_ms": {name: (ms / max(1, n)) for name, (ms, n) in prof.items()},
+        "fc2_gbs": work["fc2_bytes"] / (fc2_ms / 1e3) / 1e9 if fc2_ms > 0 else None,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(cfg, hidden, logits, W)
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="dsv4", choices=sorted(syn.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget-s", type=float, default=150.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    cfg = syn.CONFIGS[args.workload]
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        res = run_reference(args, cfg, world, rank)
+    else:
+        res = run_ours(args, cfg, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

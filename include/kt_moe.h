@@ -75,6 +75,10 @@ typedef int kt_status;
 /* Human-readable name of a status code (static string, never NULL). */
 const char* kt_status_string(kt_status status);
 
+/* Detail of the last failed call on this host thread (argument check that
+ * failed, or the CUDA error string); "" when none.  Valid until the next call. */
+const char* kt_last_error(void);
+
 /* ------------------------------------------------------------------ */
 /* Routing + permutation (route and permute steps).                   */
 /* ------------------------------------------------------------------ */
@@ -181,6 +185,34 @@ kt_status kt_mx_grouped_gemm_f32(const uint8_t* act, const uint8_t* act_sf, int 
                                  const int32_t* expert_offsets,
                                  const uint8_t* w, const uint8_t* w_sf, int E, int N,
                                  float* out, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ */
+/* Measurement hooks.                                                 */
+/* ------------------------------------------------------------------ */
+
+/* Number of kernels this library has launched in this process so far. */
+uint64_t kt_moe_kernel_launches(void);
+
+/* Stages of one layer, in launch order (index into kt_moe_profile_read). */
+#define KT_STAGE_ROUTE 0     /* top-k routing (kt_moe_route_permute only) */
+#define KT_STAGE_PERMUTE 1   /* histogram + scan + stable scatter */
+#define KT_STAGE_QUANT 2     /* MXFP8 activation quantisation + scatter */
+#define KT_STAGE_FC1 3       /* FC1 grouped GEMM + SwiGLU + MXFP8 requant */
+#define KT_STAGE_FC2 4       /* FC2 grouped GEMM + weighted store */
+#define KT_STAGE_COMBINE 5   /* top-k combine -> bf16 out */
+#define KT_NUM_STAGES 6
+
+/*
+ * Stage timing.  While enabled, every route/forward call records CUDA
+ * events on its own stream around each stage (recording adds no device
+ * work and no synchronisation).  kt_moe_profile_read synchronises on the
+ * last event, adds each stage's elapsed time over all calls since
+ * enabling into stage_ms[KT_NUM_STAGES] (host array, milliseconds) and the
+ * number of calls that ran each stage into calls[KT_NUM_STAGES].
+ * Enabling (again) discards earlier records.  Not thread-safe.
+ */
+kt_status kt_moe_profile_enable(int enable);
+kt_status kt_moe_profile_read(double* stage_ms, int* calls);
 
 /* ------------------------------------------------------------------ */
 /* Layerwise prefill: stream layer l+1's experts host -> device while  */

@@ -1,1 +1,317 @@
-"""GB300 (sm_103a) fused MXFP4-weight MoE layer -- placeholder, binding follows."""
+"""GB300 (sm_103a) fused MXFP4-weight mixture-of-experts layer.
+
+Thin Python binding over the C ABI in ``include/kt_moe.h`` (library
+``_build/libkt_moe.so``, built by ``build_ext.build``).  Every step of the
+layer runs in the library's CUDA kernels; this module only checks shapes,
+allocates outputs/workspaces with torch and passes raw device pointers and
+the current CUDA stream.  There is no CPU or torch fallback: if the library
+cannot be built or loaded, every op raises.
+
+Formats: hidden/out bf16 [T, H]; topk_ids int32 [T, k]; topk_w float32 [T, k];
+w13 uint8 fp4x2 [E, 2I, H/2] (rows [0, I) gate, [I, 2I) up; element 2i in the
+low nibble) + w13_sf uint8 e8m0 [E, 2I, H/32]; w2 uint8 fp4x2 [E, H, I/2] +
+w2_sf uint8 e8m0 [E, H, I/32].
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import build_ext
+
+__all__ = [
+    "KTError", "lib", "route_permute", "forward", "workspace_bytes", "workspace_layout", "read_device_error",
+    "grouped_gemm_f32", "Layerwise", "status_string", "check_fc_shapes", "kernel_launches", "profile_enable",
+    "profile_read", "STAGES",
+]
+
+KT_OK = 0
+KT_DEVERR_BAD_EXPERT_ID = 0x1
+KT_DEVERR_TIMEOUT_LOAD = 0x2
+KT_DEVERR_TIMEOUT_MMA = 0x4
+KT_DEVERR_TIMEOUT_EPI = 0x8
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KTError(RuntimeError):
+    def __init__(self, status: int, what: str, detail: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status}) {detail}".strip())
+
+
+class WsLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("err", "expert_offsets", "chunk_prefix", "perm", "inv_perm", "hist", "a1", "a1_sf", "a2", "a2_sf",
+                 "y", "total")]
+
+
+_VP, _SZ, _I = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+
+_SIGNATURES = {
+    "kt_status_string": ([_I], ctypes.c_char_p),
+    "kt_last_error": ([], ctypes.c_char_p),
+    "kt_moe_route_workspace_bytes": ([_I, _I, _I], _SZ),
+    "kt_moe_route_permute": ([_VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I),
+    "kt_moe_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
+    "kt_mxfp4_moe_forward": ([_VP, _I, _I, _VP, _VP, _I, _VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _SZ, _VP], _I),
+    "kt_moe_workspace_layout": ([_I, _I, _I, _I, _I, ctypes.POINTER(WsLayout)], _I),
+    "kt_moe_read_device_error": ([_VP, ctypes.POINTER(_I), _VP], _I),
+    "kt_mx_gemm_workspace_bytes": ([_I], _SZ),
+    "kt_mx_grouped_gemm_f32": ([_VP, _VP, _I, _I, _VP, _VP, _VP, _I, _I, _VP, _VP, _SZ, _VP], _I),
+    "kt_layerwise_pack_bytes": ([_I, _I, _I], _SZ),
+    "kt_layerwise_pack_offsets": ([_I, _I, _I, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ), ctypes.POINTER(_SZ),
+                                   ctypes.POINTER(_SZ)], _I),
+    "kt_layerwise_create": ([ctypes.POINTER(_VP), _I, _I, _I, _I, _I, _I, ctypes.POINTER(_VP)], _I),
+    "kt_layerwise_prefill": ([_VP, _VP, ctypes.POINTER(_VP), _VP, _I, _I, _VP], _I),
+    "kt_layerwise_inject_copy_failure": ([_VP, _I], _I),
+    "kt_layerwise_destroy": ([_VP], _I),
+    "kt_moe_kernel_launches": ([], ctypes.c_uint64),
+    "kt_moe_profile_enable": ([_I], _I),
+    "kt_moe_profile_read": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)], _I),
+}
+
+STAGES = ("route", "permute", "quant", "fc1", "fc2", "combine")
+
+
+def lib(build_if_missing: bool = True):
+    """The loaded C library (built in-tree on first use if absent)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = build_ext.build() if build_if_missing else build_ext.LIB_PATH
+            L = ctypes.CDLL(path)
+            for name, (args, res) in _SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().kt_status_string(int(status)).decode()
+    except Exception:  # noqa: BLE001 - used while formatting an error
+        return "KT_STATUS"
+
+
+def _check(status: int, what: str):
+    if status != KT_OK:
+        detail = lib().kt_last_error().decode()
+        raise KTError(status, what, detail)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream, device):
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def check_fc_shapes(w13: torch.Tensor, w2: torch.Tensor):
+    """(E, I, H) after checking that the gated FC1 inter size (rows per expert
+    of w13) is twice the FC2 inter size (2 * w2.shape[2])."""
+    E, fc1_inter, h_half = w13.shape
+    E2, H, i_half = w2.shape
+    fc2_inter = 2 * i_half
+    if E2 != E or 2 * h_half != H:
+        raise ValueError(f"w13 {tuple(w13.shape)} and w2 {tuple(w2.shape)} disagree on E or H")
+    if fc1_inter != 2 * fc2_inter:
+        raise ValueError(f"gated FC1 inter size {fc1_inter} must be twice the FC2 inter size {fc2_inter} "
+                         f"(expected {2 * fc2_inter})")
+    return E, fc2_inter, H
+
+
+def workspace_bytes(T: int, H: int, I: int, E: int, k: int) -> int:
+    return int(lib().kt_moe_workspace_bytes(T, H, I, E, k))
+
+
+def workspace_layout(T: int, H: int, I: int, E: int, k: int) -> dict:
+    L = WsLayout()
+    _check(lib().kt_moe_workspace_layout(T, H, I, E, k, ctypes.byref(L)), "kt_moe_workspace_layout")
+    return {n: int(getattr(L, n)) for n, _ in WsLayout._fields_}
+
+
+def route_permute(logits: torch.Tensor, k: int, renormalize: bool = True, stream=None, out=None, workspace=None):
+    """Top-k routing + permutation.  Returns (topk_ids, topk_w, expert_offsets, perm, inv_perm)."""
+    _need(logits, "logits", torch.float32, 2)
+    T, E = logits.shape
+    dev = logits.device
+    if out is None:
+        out = (torch.empty(T, k, dtype=torch.int32, device=dev), torch.empty(T, k, dtype=torch.float32, device=dev),
+               torch.empty(E + 1, dtype=torch.int32, device=dev), torch.empty(T * k, dtype=torch.int32, device=dev),
+               torch.empty(T * k, dtype=torch.int32, device=dev))
+    ids, w, offsets, perm, inv = out
+    nbytes = int(lib().kt_moe_route_workspace_bytes(T, E, k))
+    if nbytes == 0 and T > 0:
+        _check(lib().kt_moe_route_permute(None, T, E, k, 1, None, None, None, None, None, None, 0, None),
+               "kt_moe_route_permute")
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().kt_moe_route_permute(_ptr(logits), T, E, k, int(bool(renormalize)), _ptr(ids), _ptr(w),
+                                          _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(workspace), workspace.numel(),
+                                          _stream_ptr(stream, dev)), "kt_moe_route_permute")
+    return ids, w, offsets, perm, inv
+
+
+def forward(hidden: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, w13: torch.Tensor,
+            w13_sf: torch.Tensor, w2: torch.Tensor, w2_sf: torch.Tensor, out: torch.Tensor | None = None,
+            workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One fused MoE layer forward; returns out (bf16 [T, H])."""
+    _need(hidden, "hidden", torch.bfloat16, 2)
+    dev = hidden.device
+    _need(topk_ids, "topk_ids", torch.int32, 2, dev)
+    _need(topk_w, "topk_w", torch.float32, 2, dev)
+    for name, t in (("w13", w13), ("w13_sf", w13_sf), ("w2", w2), ("w2_sf", w2_sf)):
+        _need(t, name, torch.uint8, 3, dev)
+    E, I, H = check_fc_shapes(w13, w2)
+    T, k = topk_ids.shape
+    if hidden.shape != (T, H) or topk_w.shape != (T, k):
+        raise ValueError(f"hidden {tuple(hidden.shape)} / topk_w {tuple(topk_w.shape)} do not match "
+                         f"T={T}, H={H}, k={k}")
+    if w13_sf.shape != (E, 2 * I, H // 32) or w2_sf.shape != (E, H, I // 32):
+        raise ValueError("scale tensors must be [E, 2I, H/32] and [E, H, I/32]")
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, 2, dev)
+    nbytes = workspace_bytes(T, H, I, E, k)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().kt_mxfp4_moe_forward(_ptr(hidden), T, H, _ptr(topk_ids), _ptr(topk_w), k, _ptr(w13),
+                                          _ptr(w13_sf), _ptr(w2), _ptr(w2_sf), E, I, _ptr(out), _ptr(workspace),
+                                          workspace.numel(), _stream_ptr(stream, dev)), "kt_mxfp4_moe_forward")
+    return out
+
+
+def read_device_error(workspace: torch.Tensor, stream=None) -> int:
+    """Device error word of the last forward/route call that used `workspace`."""
+    code = ctypes.c_int(0)
+    st = lib().kt_moe_read_device_error(_ptr(workspace), ctypes.byref(code), _stream_ptr(stream, workspace.device))
+    if st not in (KT_OK, -6, -8):
+        _check(st, "kt_moe_read_device_error")
+    return code.value
+
+
+def grouped_gemm_f32(act, act_sf, expert_offsets, w, w_sf, out=None, stream=None):
+    """Diagnostic: the block-scaled grouped GEMM alone, fp32 out [S, N]."""
+    _need(act, "act", torch.uint8, 2)
+    dev = act.device
+    S, K = act.shape
+    E, N, _ = w.shape
+    if out is None:
+        out = torch.zeros(S, N, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(int(lib().kt_mx_gemm_workspace_bytes(E)), 1), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().kt_mx_grouped_gemm_f32(_ptr(act), _ptr(act_sf), S, K, _ptr(expert_offsets), _ptr(w), _ptr(w_sf),
+                                            E, N, _ptr(out), _ptr(ws), ws.numel(), _stream_ptr(stream, dev)),
+               "kt_mx_grouped_gemm_f32")
+    return out, ws
+
+
+def kernel_launches() -> int:
+    """Kernels this library has launched in this process."""
+    return int(lib().kt_moe_kernel_launches())
+
+
+def profile_enable(enable: bool = True):
+    """Start (or stop) recording per-stage CUDA events; discards old records."""
+    _check(lib().kt_moe_profile_enable(int(bool(enable))), "kt_moe_profile_enable")
+
+
+def profile_read() -> dict:
+    """{stage: (total_ms, calls)} over the calls recorded since profile_enable()."""
+    ms = (ctypes.c_double * len(STAGES))()
+    calls = (ctypes.c_int * len(STAGES))()
+    _check(lib().kt_moe_profile_read(ms, calls), "kt_moe_profile_read")
+    return {name: (float(ms[i]), int(calls[i])) for i, name in enumerate(STAGES)}
+
+
+class Layerwise:
+    """Layerwise prefill over L layers whose packed experts live in pinned host memory."""
+
+    def __init__(self, host_packs: list[torch.Tensor], H: int, I: int, E: int, k: int, T_max: int):
+        self.H, self.I, self.E, self.k, self.T_max = H, I, E, k, T_max
+        need = int(lib().kt_layerwise_pack_bytes(H, I, E))
+        for p in host_packs:
+            if p.device.type != "cpu" or not p.is_pinned() or p.dtype != torch.uint8 or p.numel() < need:
+                raise ValueError(f"each host pack must be a pinned uint8 CPU tensor of >= {need} bytes")
+        self._packs = list(host_packs)     # keep them alive
+        arr = (ctypes.c_void_p * len(host_packs))(*[p.data_ptr() for p in host_packs])
+        h = ctypes.c_void_p()
+        _check(lib().kt_layerwise_create(ctypes.byref(h), len(host_packs), H, I, E, k, T_max, arr),
+               "kt_layerwise_create")
+        self._h = h
+
+    @staticmethod
+    def pack_bytes(H: int, I: int, E: int) -> int:
+        return int(lib().kt_layerwise_pack_bytes(H, I, E))
+
+    @staticmethod
+    def pack_offsets(H: int, I: int, E: int) -> tuple[int, int, int, int]:
+        o = [ctypes.c_size_t() for _ in range(4)]
+        _check(lib().kt_layerwise_pack_offsets(H, I, E, *[ctypes.byref(x) for x in o]), "kt_layerwise_pack_offsets")
+        return tuple(int(x.value) for x in o)
+
+    @classmethod
+    def pack(cls, w13, w13_sf, w2, w2_sf, out: torch.Tensor | None = None) -> torch.Tensor:
+        """Pack one layer's weights into a pinned host buffer (w13 | w13_sf | w2 | w2_sf)."""
+        E, I, H = check_fc_shapes(w13, w2)
+        n = cls.pack_bytes(H, I, E)
+        if out is None:
+            out = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        offs = cls.pack_offsets(H, I, E)
+        for off, t in zip(offs, (w13, w13_sf, w2, w2_sf)):
+            out[off:off + t.numel()].copy_(t.reshape(-1), non_blocking=False)
+        return out
+
+    def inject_copy_failure(self, layer: int):
+        _check(lib().kt_layerwise_inject_copy_failure(self._h, layer), "kt_layerwise_inject_copy_failure")
+
+    def prefill(self, hidden: torch.Tensor, logits: list[torch.Tensor], out: torch.Tensor | None = None,
+                serialized: bool = False, stream=None) -> torch.Tensor:
+        _need(hidden, "hidden", torch.bfloat16, 2)
+        dev = hidden.device
+        T = hidden.shape[0]
+        for lg in logits:
+            _need(lg, "logits", torch.float32, 2, dev)
+        if out is None:
+            out = torch.empty_like(hidden)
+        arr = (ctypes.c_void_p * len(logits))(*[lg.data_ptr() for lg in logits])
+        with torch.cuda.device(dev):
+            _check(lib().kt_layerwise_prefill(self._h, _ptr(hidden), arr, _ptr(out), T, int(bool(serialized)),
+                                              _stream_ptr(stream, dev)), "kt_layerwise_prefill")
+        return out
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _check(lib().kt_layerwise_destroy(self._h), "kt_layerwise_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 - interpreter shutdown
+            pass

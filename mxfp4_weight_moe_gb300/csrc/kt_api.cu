@@ -1,0 +1,333 @@
+// kt_api.cu -- the C ABI declared in include/kt_moe.h: argument checks,
+// workspace carving and the launch sequence of one MoE layer forward
+// (permute -> quantise+scatter -> FC1+SwiGLU+requant -> FC2 -> combine).
+#include <cstdarg>
+#include <climits>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "kt_internal.h"
+
+namespace kt {
+
+static thread_local char g_last_error[256] = "";
+
+static kt_status fail(kt_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+static kt_status fail(kt_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+kt_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return KT_OK;
+    snprintf(g_last_error, sizeof(g_last_error), "CUDA error %d: %s", static_cast<int>(e), cudaGetErrorString(e));
+    return KT_ERR_CUDA;
+}
+
+int sm_count() {
+    static int counts[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (counts[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        counts[dev] = n > 0 ? n : 1;
+    }
+    return counts[dev];
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool ws_layout(int T, int H, int I, int E, int k, kt_ws_layout* L) {
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return false;
+    const size_t S = static_cast<size_t>(T) * static_cast<size_t>(k);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 1024);
+        return o;
+    };
+    L->err = take(256);
+    L->expert_offsets = take(sizeof(int32_t) * (E + 1));
+    L->chunk_prefix = take(sizeof(int32_t) * (E + 1));
+    L->perm = take(sizeof(int32_t) * S);
+    L->inv_perm = take(sizeof(int32_t) * S);
+    L->hist = take(sizeof(int32_t) * static_cast<size_t>(perm_tiles(static_cast<long long>(S))) * E);
+    L->a1 = take(S * H);
+    L->a1_sf = take(S * (H / 32));
+    L->a2 = take(S * I);
+    L->a2_sf = take(S * (I / 32));
+    L->y = take(S * H * sizeof(uint16_t));
+    L->total = off;
+    return true;
+}
+
+bool route_ws_layout(int T, int E, int k, RouteWs* L) {
+    if (T < 0 || E <= 0 || k <= 0) return false;
+    const long long S = static_cast<long long>(T) * k;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 1024);
+        return o;
+    };
+    L->err = take(256);
+    L->hist = take(sizeof(int32_t) * static_cast<size_t>(perm_tiles(S)) * E);
+    L->chunk_prefix = take(sizeof(int32_t) * (E + 1));
+    L->total = off;
+    return true;
+}
+
+static kt_status check_route_shape(int T, int E, int k) {
+    if (T < 0) return fail(KT_ERR_INVALID_ARG, "T=%d must be >= 0", T);
+    if (E <= 0 || k <= 0) return fail(KT_ERR_INVALID_ARG, "E=%d and k=%d must be positive", E, k);
+    if (k > E) return fail(KT_ERR_INVALID_ARG, "k=%d exceeds E=%d", k, E);
+    if (E > kMaxExperts) return fail(KT_ERR_UNSUPPORTED_SHAPE, "E=%d above the supported %d", E, kMaxExperts);
+    if (k > kMaxTopK) return fail(KT_ERR_UNSUPPORTED_SHAPE, "k=%d above the supported %d", k, kMaxTopK);
+    if (static_cast<long long>(T) * k > INT_MAX / 2)
+        return fail(KT_ERR_UNSUPPORTED_SHAPE, "T*k=%lld slots too many", static_cast<long long>(T) * k);
+    return KT_OK;
+}
+
+}  // namespace kt
+
+using namespace kt;
+
+extern "C" {
+
+const char* kt_status_string(kt_status s) {
+    switch (s) {
+        case KT_OK: return "KT_OK";
+        case KT_ERR_INVALID_ARG: return "KT_ERR_INVALID_ARG";
+        case KT_ERR_UNSUPPORTED_SHAPE: return "KT_ERR_UNSUPPORTED_SHAPE";
+        case KT_ERR_WORKSPACE: return "KT_ERR_WORKSPACE";
+        case KT_ERR_CUDA: return "KT_ERR_CUDA";
+        case KT_ERR_TIMEOUT: return "KT_ERR_TIMEOUT";
+        case KT_ERR_DEVICE_TIMEOUT: return "KT_ERR_DEVICE_TIMEOUT";
+        case KT_ERR_ALIGNMENT: return "KT_ERR_ALIGNMENT";
+        case KT_ERR_BAD_EXPERT_ID: return "KT_ERR_BAD_EXPERT_ID";
+        default: return "KT_ERR_UNKNOWN";
+    }
+}
+
+const char* kt_last_error(void) { return g_last_error; }
+
+size_t kt_moe_route_workspace_bytes(int T, int E, int k) {
+    RouteWs L;
+    if (check_route_shape(T, E, k) != KT_OK || !route_ws_layout(T, E, k, &L)) return 0;
+    return L.total;
+}
+
+kt_status kt_moe_route_permute(const float* logits, int T, int E, int k, int renormalize, int32_t* topk_ids,
+                               float* topk_w, int32_t* expert_offsets, int32_t* perm, int32_t* inv_perm, void* ws,
+                               size_t ws_bytes, void* stream) {
+    g_last_error[0] = '\0';
+    kt_status st = check_route_shape(T, E, k);
+    if (st != KT_OK) return st;
+    if (T == 0) return KT_OK;
+    if (!logits || !topk_ids || !topk_w || !expert_offsets || !perm || !inv_perm || !ws)
+        return fail(KT_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(expert_offsets, 4) ||
+        !aligned(perm, 4) || !aligned(inv_perm, 4))
+        return fail(KT_ERR_ALIGNMENT, "routing pointers must be 4-byte aligned");
+    RouteWs L;
+    route_ws_layout(T, E, k, &L);
+    if (!aligned(ws, 256)) return fail(KT_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (ws_bytes < L.total) return fail(KT_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, L.total);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    int* err = reinterpret_cast<int*>(base + L.err);
+    if ((st = cuda_status(cudaMemsetAsync(err, 0, sizeof(int), s))) != KT_OK) return st;
+    {
+        StageTimer timer(KT_STAGE_ROUTE, s);
+        if ((st = cuda_status(launch_route_topk(logits, T, E, k, renormalize ? 1 : 0, topk_ids, topk_w, s))) !=
+            KT_OK)
+            return st;
+    }
+    StageTimer timer(KT_STAGE_PERMUTE, s);
+    return cuda_status(launch_permute(topk_ids, static_cast<long long>(T) * k, E,
+                                      reinterpret_cast<int32_t*>(base + L.hist), expert_offsets,
+                                      reinterpret_cast<int32_t*>(base + L.chunk_prefix), perm, inv_perm, err, s));
+}
+
+size_t kt_moe_workspace_bytes(int T, int H, int I, int E, int k) {
+    kt_ws_layout L;
+    if (check_route_shape(T, E, k) != KT_OK) return 0;
+    if (H <= 0 || I <= 0 || H % 128 || I % 128) return 0;
+    if (!ws_layout(T, H, I, E, k, &L)) return 0;
+    return L.total;
+}
+
+kt_status kt_moe_workspace_layout(int T, int H, int I, int E, int k, kt_ws_layout* layout) {
+    if (!layout) return fail(KT_ERR_INVALID_ARG, "null layout");
+    if (kt_moe_workspace_bytes(T, H, I, E, k) == 0 && T != 0)
+        return fail(KT_ERR_UNSUPPORTED_SHAPE, "invalid sizes");
+    if (!ws_layout(T, H, I, E, k, layout)) return fail(KT_ERR_INVALID_ARG, "invalid sizes");
+    return KT_OK;
+}
+
+kt_status kt_mxfp4_moe_forward(const uint16_t* hidden, int T, int H, const int32_t* topk_ids, const float* topk_w,
+                               int k, const uint8_t* w13, const uint8_t* w13_sf, const uint8_t* w2,
+                               const uint8_t* w2_sf, int E, int I, uint16_t* out, void* ws, size_t ws_bytes,
+                               void* stream) {
+    g_last_error[0] = '\0';
+    kt_status st = check_route_shape(T, E, k);
+    if (st != KT_OK) return st;
+    if (H <= 0 || I <= 0) return fail(KT_ERR_INVALID_ARG, "H=%d and I=%d must be positive", H, I);
+    if (H % 128 || I % 128)
+        return fail(KT_ERR_UNSUPPORTED_SHAPE, "H=%d and I=%d must be multiples of 128", H, I);
+    if (static_cast<long long>(E) * 2 * I > INT_MAX / 2 || static_cast<long long>(E) * H > INT_MAX / 2)
+        return fail(KT_ERR_UNSUPPORTED_SHAPE, "E*2I or E*H too large");
+    if (T == 0) return KT_OK;
+    if (!hidden || !topk_ids || !topk_w || !w13 || !w13_sf || !w2 || !w2_sf || !out || !ws)
+        return fail(KT_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(hidden, 16) || !aligned(out, 16) || !aligned(topk_ids, 16) || !aligned(topk_w, 16))
+        return fail(KT_ERR_ALIGNMENT, "hidden, out, topk_ids and topk_w must be 16-byte aligned");
+    if (!aligned(w13, 32) || !aligned(w2, 32))
+        return fail(KT_ERR_ALIGNMENT, "w13 and w2 must be 32-byte aligned");
+    if (!aligned(w13_sf, 16) || !aligned(w2_sf, 16))
+        return fail(KT_ERR_ALIGNMENT, "w13_sf and w2_sf must be 16-byte aligned");
+    kt_ws_layout L;
+    ws_layout(T, H, I, E, k, &L);
+    if (!aligned(ws, 256)) return fail(KT_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (ws_bytes < L.total) return fail(KT_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, L.total);
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    int* err = reinterpret_cast<int*>(base + L.err);
+    int32_t* offsets = reinterpret_cast<int32_t*>(base + L.expert_offsets);
+    int32_t* chunk_prefix = reinterpret_cast<int32_t*>(base + L.chunk_prefix);
+    int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
+    int32_t* inv_perm = reinterpret_cast<int32_t*>(base + L.inv_perm);
+    uint8_t* a1 = base + L.a1;
+    uint8_t* a1_sf = base + L.a1_sf;
+    uint8_t* a2 = base + L.a2;
+    uint8_t* a2_sf = base + L.a2_sf;
+    uint16_t* y = reinterpret_cast<uint16_t*>(base + L.y);
+    const long long S = static_cast<long long>(T) * k;
+
+    if ((st = cuda_status(cudaMemsetAsync(err, 0, sizeof(int), s))) != KT_OK) return st;
+    {
+        StageTimer timer(KT_STAGE_PERMUTE, s);
+        if ((st = cuda_status(launch_permute(topk_ids, S, E, reinterpret_cast<int32_t*>(base + L.hist), offsets,
+                                             chunk_prefix, perm, inv_perm, err, s))) != KT_OK)
+            return st;
+    }
+    {
+        StageTimer timer(KT_STAGE_QUANT, s);
+        if ((st = cuda_status(launch_quant_scatter(hidden, T, H, k, inv_perm, a1, a1_sf, s))) != KT_OK) return st;
+    }
+
+    GemmArgs fc1{};
+    fc1.mode = GemmEpilogue::SwiGLU;
+    fc1.expert_offsets = offsets;
+    fc1.chunk_prefix = chunk_prefix;
+    fc1.E = E;
+    fc1.K = H;
+    fc1.rows_w = 2 * I;
+    fc1.I = I;
+    fc1.S = static_cast<int>(S);
+    fc1.H = H;
+    fc1.w = w13;
+    fc1.w_sf = w13_sf;
+    fc1.act = a1;
+    fc1.act_sf = a1_sf;
+    fc1.a2 = a2;
+    fc1.a2_sf = a2_sf;
+    fc1.err = err;
+    {
+        StageTimer timer(KT_STAGE_FC1, s);
+        if ((st = launch_gemm(fc1, s)) != KT_OK) return st;
+    }
+
+    GemmArgs fc2{};
+    fc2.mode = GemmEpilogue::Combine;
+    fc2.expert_offsets = offsets;
+    fc2.chunk_prefix = chunk_prefix;
+    fc2.E = E;
+    fc2.K = I;
+    fc2.rows_w = H;
+    fc2.I = I;
+    fc2.S = static_cast<int>(S);
+    fc2.H = H;
+    fc2.w = w2;
+    fc2.w_sf = w2_sf;
+    fc2.act = a2;
+    fc2.act_sf = a2_sf;
+    fc2.y = y;
+    fc2.perm = perm;
+    fc2.topk_w = topk_w;
+    fc2.err = err;
+    {
+        StageTimer timer(KT_STAGE_FC2, s);
+        if ((st = launch_gemm(fc2, s)) != KT_OK) return st;
+    }
+    StageTimer timer(KT_STAGE_COMBINE, s);
+    return cuda_status(launch_combine(y, topk_ids, T, H, k, E, out, s));
+}
+
+kt_status kt_moe_read_device_error(const void* ws, int* code, void* stream) {
+    g_last_error[0] = '\0';
+    if (!ws || !code) return fail(KT_ERR_INVALID_ARG, "null pointer argument");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    kt_status st = cuda_status(cudaStreamSynchronize(s));
+    if (st != KT_OK) return st;
+    int v = 0;
+    if ((st = cuda_status(cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost))) != KT_OK) return st;
+    *code = v;
+    if (v & (KT_DEVERR_TIMEOUT_LOAD | KT_DEVERR_TIMEOUT_MMA | KT_DEVERR_TIMEOUT_EPI))
+        return fail(KT_ERR_DEVICE_TIMEOUT, "device error word 0x%x", v);
+    if (v & KT_DEVERR_BAD_EXPERT_ID) return fail(KT_ERR_BAD_EXPERT_ID, "device error word 0x%x", v);
+    return KT_OK;
+}
+
+size_t kt_mx_gemm_workspace_bytes(int E) {
+    if (E <= 0 || E > kMaxExperts) return 0;
+    return 1024 + align_up(sizeof(int32_t) * (E + 1), 1024);
+}
+
+kt_status kt_mx_grouped_gemm_f32(const uint8_t* act, const uint8_t* act_sf, int S, int K,
+                                 const int32_t* expert_offsets, const uint8_t* w, const uint8_t* w_sf, int E, int N,
+                                 float* out, void* ws, size_t ws_bytes, void* stream) {
+    g_last_error[0] = '\0';
+    if (S < 0 || K <= 0 || N <= 0 || E <= 0) return fail(KT_ERR_INVALID_ARG, "invalid sizes");
+    if (K % 128 || N % 128) return fail(KT_ERR_UNSUPPORTED_SHAPE, "K=%d and N=%d must be multiples of 128", K, N);
+    if (E > kMaxExperts) return fail(KT_ERR_UNSUPPORTED_SHAPE, "E=%d above the supported %d", E, kMaxExperts);
+    if (S == 0) return KT_OK;
+    if (!act || !act_sf || !expert_offsets || !w || !w_sf || !out || !ws)
+        return fail(KT_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(act, 16) || !aligned(w, 32) || !aligned(act_sf, 4) || !aligned(w_sf, 4) || !aligned(out, 16))
+        return fail(KT_ERR_ALIGNMENT, "misaligned pointer");
+    if (!aligned(ws, 256)) return fail(KT_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (ws_bytes < kt_mx_gemm_workspace_bytes(E)) return fail(KT_ERR_WORKSPACE, "workspace too small");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    int* err = reinterpret_cast<int*>(base);
+    int32_t* chunk_prefix = reinterpret_cast<int32_t*>(base + 1024);
+    kt_status st;
+    if ((st = cuda_status(cudaMemsetAsync(err, 0, sizeof(int), s))) != KT_OK) return st;
+    if ((st = cuda_status(launch_chunk_prefix(expert_offsets, E, chunk_prefix, s))) != KT_OK) return st;
+    GemmArgs g{};
+    g.mode = GemmEpilogue::Raw;
+    g.expert_offsets = expert_offsets;
+    g.chunk_prefix = chunk_prefix;
+    g.E = E;
+    g.K = K;
+    g.rows_w = N;
+    g.I = 0;
+    g.S = S;
+    g.H = 0;
+    g.w = w;
+    g.w_sf = w_sf;
+    g.act = act;
+    g.act_sf = act_sf;
+    g.raw_out = out;
+    g.err = err;
+    return launch_gemm(g, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,106 @@
+// kt_internal.h -- host-side declarations shared by the library's
+// translation units: workspace layout, kernel launchers and tensor maps.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kt_moe.h"
+
+namespace kt {
+
+// Token rows of one GEMM tile (the MMA N extent, at most 256) and the number
+// of slots one permutation tile handles.
+constexpr int kTileTokens = 256;
+constexpr int kPermTile = 1024;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline int perm_tiles(long long S) { return static_cast<int>((S + kPermTile - 1) / kPermTile); }
+
+// Workspace carving (offsets relative to the 256-byte aligned base).
+bool ws_layout(int T, int H, int I, int E, int k, kt_ws_layout* L);
+// Routing workspace: error word, hist [tiles * E], chunk prefix [E + 1].
+struct RouteWs {
+    size_t err, hist, chunk_prefix, total;
+};
+bool route_ws_layout(int T, int E, int k, RouteWs* L);
+
+// ------------------------------------------------------------- launchers
+// All return cudaSuccess or the launch error; none synchronises.
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renormalize, int32_t* ids, float* w,
+                              cudaStream_t s);
+// Permutation of S = T*k slots: histogram -> scan -> stable scatter.
+// Writes expert_offsets [E+1], chunk_prefix [E+1] (token chunks of at most
+// kTileTokens rows per expert), perm [S], inv_perm [S]; hist is scratch of
+// perm_tiles(S) * E ints; err collects KT_DEVERR_BAD_EXPERT_ID.
+cudaError_t launch_permute(const int32_t* ids, long long S, int E, int32_t* hist, int32_t* expert_offsets,
+                           int32_t* chunk_prefix, int32_t* perm, int32_t* inv_perm, int* err, cudaStream_t s);
+// chunk_prefix [E+1] from expert_offsets alone (for the diagnostic GEMM).
+cudaError_t launch_chunk_prefix(const int32_t* expert_offsets, int E, int32_t* chunk_prefix, cudaStream_t s);
+// MXFP8 quantisation of hidden rows, each written to its k permuted rows.
+cudaError_t launch_quant_scatter(const uint16_t* hidden, int T, int H, int k, const int32_t* inv_perm, uint8_t* a1,
+                                 uint8_t* a1_sf, cudaStream_t s);
+// out[t] = sum over valid slots of y[t*k + j] (y already weighted).
+cudaError_t launch_combine(const uint16_t* y, const int32_t* ids, int T, int H, int k, int E, uint16_t* out,
+                           cudaStream_t s);
+
+enum class GemmEpilogue : int { Raw = 0, SwiGLU = 1, Combine = 2 };
+
+struct GemmArgs {
+    GemmEpilogue mode;
+    const int32_t* expert_offsets;  // [E+1] permuted row ranges
+    const int32_t* chunk_prefix;    // [E+1]
+    int E;
+    int K;            // contraction length, % 128 == 0
+    int rows_w;       // weight rows per expert (2I for FC1, H for FC2, N for Raw)
+    int I;            // FC2 inter size (SwiGLU: up rows start at I)
+    int S;            // activation rows
+    const uint8_t* w;      // fp4x2 [E, rows_w, K/2]
+    const uint8_t* w_sf;   // e8m0  [E, rows_w, K/32]
+    const uint8_t* act;    // e4m3  [S, K]
+    const uint8_t* act_sf; // e8m0  [S, K/32]
+    // SwiGLU outputs: A2 e4m3 [S, I] + e8m0 [S, I/32]
+    uint8_t* a2;
+    uint8_t* a2_sf;
+    // Combine outputs: y bf16 [S, H] in slot order, scaled by topk_w
+    uint16_t* y;
+    const int32_t* perm;
+    const float* topk_w;
+    int H;
+    // Raw output: f32 [S, rows_w]
+    float* raw_out;
+    int* err;
+};
+
+// Encodes the tensor maps and launches the persistent tcgen05 GEMM.
+// Returns KT_OK, KT_ERR_CUDA (launch / map encoding failure).
+kt_status launch_gemm(const GemmArgs& a, cudaStream_t s);
+
+// Device properties cached per device.
+int sm_count();
+
+// Status helper: map a CUDA error to KT_ERR_CUDA, remembering the last one.
+kt_status cuda_status(cudaError_t e);
+
+// Measurement hooks (kt_profile.cpp): launch counter and, when profiling is
+// enabled, CUDA events recorded on the stream around one stage (RAII).
+void count_launches(int n);
+class StageTimer {
+  public:
+    StageTimer(int stage, cudaStream_t s);
+    ~StageTimer();
+    StageTimer(const StageTimer&) = delete;
+    StageTimer& operator=(const StageTimer&) = delete;
+
+  private:
+    int stage_;
+    cudaStream_t s_;
+    cudaEvent_t end_;
+};
+
+}  // namespace kt

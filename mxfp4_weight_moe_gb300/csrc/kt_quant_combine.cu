@@ -1,0 +1,124 @@
+// kt_quant_combine.cu -- the HBM-bound ends of the layer: MXFP8 activation
+// quantisation fused with the permuted scatter, and the final top-k combine.
+//
+// MXFP8 (e4m3 elements, one e8m0 scale per 32 along H) is the activation
+// format of the "MXFP8 activation x MXFP4 weight fused MoE" ("Kimi-K3 SM120
+// FlashInfer MXFP4 MoE", Goal).  The shared exponent follows the OCP MX v1.0
+// rule floor(log2 amax) - 8 and elements are converted with round-to-
+// nearest-even, saturating at +-448.
+#include "kt_common.cuh"
+#include "kt_internal.h"
+
+namespace kt {
+
+// One warp per token row.  Lane l quantises 32-element blocks l, l+32, ...
+// (64 contiguous input bytes each) and writes the 32 codes + scale byte to
+// every permuted row the token's k slots map to.
+__global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __restrict__ hidden, int T, int H, int k,
+                                                            const int32_t* __restrict__ inv_perm,
+                                                            uint8_t* __restrict__ a1, uint8_t* __restrict__ a1_sf) {
+    __shared__ int s_dst[8][kMaxTopK];
+    const int wib = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + wib;
+    if (t >= T) return;   // whole warp
+    if (lane < k) s_dst[wib][lane] = inv_perm[static_cast<size_t>(t) * k + lane];
+    __syncwarp();
+    const int nblk = H >> 5;
+    const uint16_t* row = hidden + static_cast<size_t>(t) * H;
+    for (int b = lane; b < nblk; b += 32) {
+        const uint4* src = reinterpret_cast<const uint4*>(row + b * 32);
+        uint32_t wv[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 q = src[i];
+            wv[4 * i + 0] = q.x;
+            wv[4 * i + 1] = q.y;
+            wv[4 * i + 2] = q.z;
+            wv[4 * i + 3] = q.w;
+        }
+        float x[32];
+        uint32_t amax = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            x[2 * i] = __uint_as_float(wv[i] << 16);
+            x[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+            amax = max(amax, __float_as_uint(x[2 * i]) & 0x7FFFFFFFu);
+            amax = max(amax, __float_as_uint(x[2 * i + 1]) & 0x7FFFFFFFu);
+        }
+        const int X = mx_e4m3_block_exponent(amax);
+        const float sc = exp2_neg(X);
+        uint32_t codes[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = f32x2_to_e4m3x2_satfinite(x[4 * i] * sc, x[4 * i + 1] * sc);
+            const uint32_t hi = f32x2_to_e4m3x2_satfinite(x[4 * i + 2] * sc, x[4 * i + 3] * sc);
+            codes[i] = lo | (hi << 16);
+        }
+        const uint8_t sbyte = static_cast<uint8_t>(X + 127);
+        for (int j = 0; j < k; ++j) {
+            const int p = s_dst[wib][j];
+            if (p < 0) continue;
+            uint4* dst = reinterpret_cast<uint4*>(a1 + static_cast<size_t>(p) * H + b * 32);
+            dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+            dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+            a1_sf[static_cast<size_t>(p) * nblk + b] = sbyte;
+        }
+    }
+}
+
+cudaError_t launch_quant_scatter(const uint16_t* hidden, int T, int H, int k, const int32_t* inv_perm, uint8_t* a1,
+                                 uint8_t* a1_sf, cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    quant_scatter_kernel<<<(T + 7) / 8, 256, 0, s>>>(hidden, T, H, k, inv_perm, a1, a1_sf);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// out[t, h] = bf16( sum_j y[t*k + j, h] ) over slots with a valid id, summed
+// in fp32 in slot order (y rows were already multiplied by topk_w).
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ ids,
+                                                      int T, int H, int k, int E, uint16_t* __restrict__ out) {
+    const int h8n = H >> 3;
+    const long long n = static_cast<long long>(T) * h8n;
+    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int t = static_cast<int>(idx / h8n);
+        const int h8 = static_cast<int>(idx % h8n);
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int e = ids[static_cast<size_t>(t) * k + j];
+            if (e < 0 || e >= E) continue;
+            const uint4 q = *reinterpret_cast<const uint4*>(y + (static_cast<size_t>(t) * k + j) * H + h8 * 8);
+            const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] += __uint_as_float(wv[i] << 16);
+                acc[2 * i + 1] += __uint_as_float(wv[i] & 0xFFFF0000u);
+            }
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+            o[i] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        *reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H + h8 * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+cudaError_t launch_combine(const uint16_t* y, const int32_t* ids, int T, int H, int k, int E, uint16_t* out,
+                           cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    const long long n = static_cast<long long>(T) * (H / 8);
+    long long blocks = (n + 255) / 256;
+    const long long cap = static_cast<long long>(sm_count()) * 8;
+    if (blocks > cap) blocks = cap;
+    combine_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(y, ids, T, H, k, E, out);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace kt

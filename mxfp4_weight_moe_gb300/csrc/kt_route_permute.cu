@@ -1,0 +1,269 @@
+// kt_route_permute.cu -- route (top-k + softmax weights) and the
+// deterministic token-to-expert permutation.
+//
+// Routing follows the top-k expert selection of the DeepSeek-V4-Flash
+// (256 experts, top-6) and Kimi-K3 (896 experts, top-16) MoE layers named in
+// "[MXFP4 layerwise prefill] SM 8.6 (Ampere) excluded by capability
+// whitelist" (Environment) and "Kimi-K3 SM120 FlashInfer MXFP4 MoE" (Phase 0
+// audit table).  The permutation groups slots by expert so that each expert's
+// rows are contiguous ("different expert hits", Kimi-K3 README, later hard
+// gates, item 5); within an expert, rows keep slot order, which makes every
+// index bit-reproducible.
+#include <cmath>
+
+#include "kt_common.cuh"
+#include "kt_internal.h"
+
+namespace kt {
+
+// ------------------------------------------------------------------ route
+// One warp per token.  Lane l holds logits l, l+32, ...; k rounds of a warp
+// arg-max (value descending, index ascending) pick the experts in order.
+// Weights are exp(l_j - l_max) / sum in fp64 (the difference of two f32
+// logits is exact in fp64), then rounded to f32.
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                         int renormalize, int32_t* __restrict__ ids,
+                                                         float* __restrict__ w) {
+    const int t = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const float* row = logits + static_cast<size_t>(t) * E;
+    const int epl = (E + 31) >> 5;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = (i < epl && e < E) ? row[e] : -INFINITY;
+    }
+    constexpr int kNone = 0x7fffffff;
+    uint32_t taken = 0;
+    int my_id = 0;
+    float my_v = 0.f;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = kNone;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int e = lane + 32 * i;
+            if (i < epl && e < E && !((taken >> i) & 1u)) {
+                if (bi == kNone || v[i] > bv) {
+                    bv = v[i];
+                    bi = e;
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (oi != kNone && (bi == kNone || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == j) {
+            my_id = bi;
+            my_v = bv;
+        }
+    }
+    const double lmax = static_cast<double>(__shfl_sync(0xffffffffu, my_v, 0));
+    const double ex = (lane < k) ? exp(static_cast<double>(my_v) - lmax) : 0.0;
+    double part = 0.0;
+    if (renormalize) {
+        part = ex;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int e = lane + 32 * i;
+            if (i < epl && e < E) part += exp(static_cast<double>(v[i]) - lmax);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    if (lane < k) {
+        ids[static_cast<size_t>(t) * k + lane] = my_id;
+        w[static_cast<size_t>(t) * k + lane] = static_cast<float>(ex / part);
+    }
+}
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renormalize, int32_t* ids, float* w,
+                              cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    const int blocks = (T + 7) / 8;
+    route_topk_kernel<<<blocks, 256, 0, s>>>(logits, T, E, k, renormalize, ids, w);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ permute
+// Pass 1: per-tile expert histogram (tile = kPermTile consecutive slots).
+__global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restrict__ ids, long long S, int E,
+                                                        int32_t* __restrict__ hist, int* err) {
+    extern __shared__ int sh_count[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) sh_count[e] = 0;
+    __syncthreads();
+    const long long base = static_cast<long long>(blockIdx.x) * kPermTile;
+    int bad = 0;
+    for (int i = threadIdx.x; i < kPermTile; i += blockDim.x) {
+        const long long s = base + i;
+        if (s < S) {
+            const int e = ids[s];
+            if (e >= 0 && e < E) atomicAdd(&sh_count[e], 1);
+            else bad = 1;
+        }
+    }
+    if (bad) set_error(err, KT_DEVERR_BAD_EXPERT_ID);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<size_t>(blockIdx.x) * E + e] = sh_count[e];
+}
+
+// Exclusive scan over the 1024 threads of a block; returns the thread's
+// exclusive prefix and writes the block total to *total (all threads).
+__device__ __forceinline__ int block_exclusive_scan_1024(int x, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += y;
+    }
+    if (lane == 31) s_warp[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int wv = s_warp[lane];
+        int winc = wv;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, winc, off);
+            if (lane >= off) winc += y;
+        }
+        s_warp[lane] = winc - wv;                 // exclusive prefix of warp totals
+        if (lane == 31) s_warp[32] = winc;        // block total
+    }
+    __syncthreads();
+    const int res = s_warp[warp] + inc - x;
+    *total = s_warp[32];
+    __syncthreads();
+    return res;
+}
+
+// Pass 2 (one block of 1024 threads, thread = expert): in-place exclusive
+// prefix of each expert's tile counts, expert offsets, token-chunk prefix.
+__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ hist, int ntiles, int E, long long S,
+                                                         int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ chunk_prefix,
+                                                         int32_t* __restrict__ perm) {
+    __shared__ int s_warp[33];
+    const int e = threadIdx.x;
+    int run = 0;
+    if (e < E) {
+        for (int t0 = 0; t0 < ntiles; t0 += 8) {
+            int h[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) h[u] = (t0 + u < ntiles) ? hist[static_cast<size_t>(t0 + u) * E + e] : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (t0 + u < ntiles) {
+                    hist[static_cast<size_t>(t0 + u) * E + e] = run;
+                    run += h[u];
+                }
+            }
+        }
+    }
+    const int cnt = (e < E) ? run : 0;
+    const int nch = (cnt + kTileTokens - 1) / kTileTokens;
+    int total_cnt, total_ch;
+    const int off = block_exclusive_scan_1024(cnt, s_warp, &total_cnt);
+    const int cpre = block_exclusive_scan_1024(nch, s_warp, &total_ch);
+    if (e < E) {
+        offsets[e] = off;
+        chunk_prefix[e] = cpre;
+    }
+    if (e == 0) {
+        offsets[E] = total_cnt;
+        chunk_prefix[E] = total_ch;
+    }
+    for (long long p = total_cnt + threadIdx.x; p < S; p += blockDim.x) perm[p] = -1;
+}
+
+// Pass 3 (one warp per tile): stable ranks inside the tile by a warp-serial
+// sweep in slot order; the peers of a slot in one 32-slot round are found
+// with match.any, so equal experts keep their slot order.
+__global__ void __launch_bounds__(32) perm_scatter_kernel(const int32_t* __restrict__ ids, long long S, int E,
+                                                          const int32_t* __restrict__ tile_base,
+                                                          const int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ perm,
+                                                          int32_t* __restrict__ inv_perm) {
+    extern __shared__ int sh_run[];
+    const int lane = threadIdx.x;
+    for (int e = lane; e < E; e += 32) sh_run[e] = 0;
+    __syncwarp();
+    const long long base = static_cast<long long>(blockIdx.x) * kPermTile;
+    const int32_t* tb = tile_base + static_cast<size_t>(blockIdx.x) * E;
+    for (int r = 0; r < kPermTile / 32; ++r) {
+        const long long s = base + r * 32 + lane;
+        if (base + r * 32 >= S) break;   // warp-uniform
+        const int e = (s < S) ? ids[s] : -1;
+        const bool valid = (s < S) && e >= 0 && e < E;
+        const int key = valid ? e : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        const int leader = __ffs(peers) - 1;
+        const int before = valid ? sh_run[e] : 0;
+        __syncwarp();
+        if (valid && lane == leader) sh_run[e] = before + __popc(peers);
+        __syncwarp();
+        if (s < S) {
+            if (valid) {
+                const int p = offsets[e] + tb[e] + before + rank;
+                perm[p] = static_cast<int32_t>(s);
+                inv_perm[s] = p;
+            } else {
+                inv_perm[s] = -1;
+            }
+        }
+    }
+}
+
+cudaError_t launch_permute(const int32_t* ids, long long S, int E, int32_t* hist, int32_t* expert_offsets,
+                           int32_t* chunk_prefix, int32_t* perm, int32_t* inv_perm, int* err, cudaStream_t s) {
+    const int ntiles = perm_tiles(S);
+    if (ntiles > 0) {
+        perm_hist_kernel<<<ntiles, 256, E * sizeof(int), s>>>(ids, S, E, hist, err);
+        count_launches(1);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    perm_scan_kernel<<<1, 1024, 0, s>>>(hist, ntiles, E, S, expert_offsets, chunk_prefix, perm);
+    count_launches(1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (ntiles > 0) {
+        perm_scatter_kernel<<<ntiles, 32, E * sizeof(int), s>>>(ids, S, E, hist, expert_offsets, perm, inv_perm);
+        count_launches(1);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+// Token-chunk prefix from expert offsets alone (one block, thread = expert).
+__global__ void __launch_bounds__(1024) chunk_prefix_kernel(const int32_t* __restrict__ offsets, int E,
+                                                            int32_t* __restrict__ chunk_prefix) {
+    __shared__ int s_warp[33];
+    const int e = threadIdx.x;
+    const int cnt = (e < E) ? offsets[e + 1] - offsets[e] : 0;
+    const int nch = cnt > 0 ? (cnt + kTileTokens - 1) / kTileTokens : 0;
+    int total;
+    const int cpre = block_exclusive_scan_1024(nch, s_warp, &total);
+    if (e < E) chunk_prefix[e] = cpre;
+    if (e == 0) chunk_prefix[E] = total;
+}
+
+cudaError_t launch_chunk_prefix(const int32_t* expert_offsets, int E, int32_t* chunk_prefix, cudaStream_t s) {
+    chunk_prefix_kernel<<<1, 1024, 0, s>>>(expert_offsets, E, chunk_prefix);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace kt

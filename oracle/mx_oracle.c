@@ -273,23 +273,31 @@ int mxo_permute(const int32_t* ids, int T, int k, int E, int32_t* offsets, int32
 
 /* One output of an MXFP8 x MXFP4 contraction over K (K % 32 == 0):
  *   sum_b 2^(sa_b-127) * 2^(sw_b-127) * sum_{i<32} a[32b+i] * w[32b+i]
- * a: e4m3 codes, sa: e8m0 bytes; w: packed e2m1 (element 2i low nibble of
- * byte i), sw: e8m0 bytes.  fp64; every product and block sum is exact. */
-static double dot_mxfp8_mxfp4(const uint8_t* a, const uint8_t* sa, const uint8_t* w, const uint8_t* sw, int K)
+ * a_val: the e4m3 elements already decoded to doubles, sa: their e8m0
+ * bytes; w: packed e2m1 (element 2i low nibble of byte i), sw: e8m0 bytes.
+ * fp64; every product and block sum is exact. */
+static double dot_mxfp8_mxfp4(const double* a_val, const uint8_t* sa, const uint8_t* w, const uint8_t* sw, int K)
 {
-    double acc = 0.0;
+    double e2m1[16], acc = 0.0;
     int b, i;
+    for (i = 0; i < 16; ++i) e2m1[i] = mxo_e2m1_value((unsigned)i);
     for (b = 0; b < K / 32; ++b) {
         double blk = 0.0;
         for (i = 0; i < 32; ++i) {
             int kk = 32 * b + i;
             unsigned byte = w[kk / 2];
             unsigned nib = (kk & 1) ? (byte >> 4) : (byte & 15u);
-            blk += mxo_e4m3_value(a[kk]) * mxo_e2m1_value(nib);
+            blk += a_val[kk] * e2m1[nib];
         }
         acc += mxo_e8m0_value(sa[b]) * mxo_e8m0_value(sw[b]) * blk;
     }
     return acc;
+}
+
+static void decode_e4m3_row(const uint8_t* codes, int n, double* out)
+{
+    int i;
+    for (i = 0; i < n; ++i) out[i] = mxo_e4m3_value(codes[i]);
 }
 
 static int scales_finite(const uint8_t* s, size_t n)
@@ -312,9 +320,13 @@ int mxo_gemm_mxfp8_mxfp4(const uint8_t* a, const uint8_t* a_sf, int M, int K,
 #pragma omp parallel for schedule(dynamic)
     for (m = 0; m < M; ++m) {
         int n;
+        double* av = (double*)malloc(sizeof(double) * (size_t)K);
+        if (!av) continue;
+        decode_e4m3_row(a + (size_t)m * K, K, av);
         for (n = 0; n < N; ++n)
-            out[(size_t)m * N + n] = dot_mxfp8_mxfp4(a + (size_t)m * K, a_sf + (size_t)m * (K / 32),
+            out[(size_t)m * N + n] = dot_mxfp8_mxfp4(av, a_sf + (size_t)m * (K / 32),
                                                      w + (size_t)n * (K / 2), w_sf + (size_t)n * (K / 32), K);
+        free(av);
     }
     return MXO_OK;
 }
@@ -363,16 +375,19 @@ int mxo_moe_forward_tokens(const uint16_t* hidden, int T, int H,
         double* acc = (double*)malloc(sizeof(double) * (size_t)2 * I);
         double* h = (double*)malloc(sizeof(double) * (size_t)I);
         double* sum = (double*)calloc((size_t)H, sizeof(double));
+        double* av = (double*)malloc(sizeof(double) * (size_t)H);
+        double* a2v = (double*)malloc(sizeof(double) * (size_t)I);
         uint8_t* a = (uint8_t*)malloc((size_t)H);
         uint8_t* sa = (uint8_t*)malloc((size_t)H / 32);
         uint8_t* a2 = (uint8_t*)malloc((size_t)I);
         uint8_t* sa2 = (uint8_t*)malloc((size_t)I / 32);
-        if (!x || !acc || !h || !sum || !a || !sa || !a2 || !sa2) {
+        if (!x || !acc || !h || !sum || !av || !a2v || !a || !sa || !a2 || !sa2) {
 #pragma omp atomic write
             err = MXO_ERR_NOMEM;
         } else {
             for (i = 0; i < H; ++i) x[i] = mxo_bf16_value(hidden[(size_t)t * H + i]);
             mxo_quant_mxfp8(x, H, a, sa);
+            decode_e4m3_row(a, H, av);
             for (j = 0; j < k; ++j) {
                 int e = ids[(size_t)t * k + j];
                 double wj = (double)topk_w[(size_t)t * k + j];
@@ -385,18 +400,19 @@ int mxo_moe_forward_tokens(const uint16_t* hidden, int T, int H,
                 }
                 for (n = 0; n < 2 * I; ++n) {
                     size_t row = (size_t)e * 2 * I + n;
-                    acc[n] = dot_mxfp8_mxfp4(a, sa, w13 + row * (H / 2), w13_sf + row * (H / 32), H);
+                    acc[n] = dot_mxfp8_mxfp4(av, sa, w13 + row * (H / 2), w13_sf + row * (H / 32), H);
                 }
                 for (i = 0; i < I; ++i) {
                     double g = acc[i], u = acc[I + i];
                     h[i] = g / (1.0 + exp(-g)) * u;
                 }
                 mxo_quant_mxfp8(h, I, a2, sa2);
+                decode_e4m3_row(a2, I, a2v);
                 if (a2_out) memcpy(a2_out + ((size_t)ti * k + j) * I, a2, (size_t)I);
                 if (a2_sf_out) memcpy(a2_sf_out + ((size_t)ti * k + j) * (I / 32), sa2, (size_t)I / 32);
                 for (n = 0; n < H; ++n) {
                     size_t row = (size_t)e * H + n;
-                    double y = dot_mxfp8_mxfp4(a2, sa2, w2 + row * (I / 2), w2_sf + row * (I / 32), I);
+                    double y = dot_mxfp8_mxfp4(a2v, sa2, w2 + row * (I / 2), w2_sf + row * (I / 32), I);
                     if (y_out) y_out[((size_t)ti * k + j) * H + n] = y;
                     sum[n] += wj * y;
                 }
@@ -406,7 +422,7 @@ int mxo_moe_forward_tokens(const uint16_t* hidden, int T, int H,
                 if (out) out[(size_t)ti * H + n] = mxo_bf16_round(sum[n]);
             }
         }
-        free(x); free(acc); free(h); free(sum); free(a); free(sa); free(a2); free(sa2);
+        free(x); free(acc); free(h); free(sum); free(av); free(a2v); free(a); free(sa); free(a2); free(sa2);
     }
     return err;
 }

@@ -1,0 +1,76 @@
+"""GPU: layerwise prefill (double-buffered host -> device expert streaming).
+
+The streamed result must be bit-identical to calling route + forward layer
+by layer with device-resident weights, and to the serialized control
+("upload all experts -> compute -> synchronise" per layer); a short chain is
+also compared with the oracle run layer by layer on its own outputs.  A copy
+failure injected on the host must drain both streams and surface as an
+error, leaving the context usable.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mxfp4_weight_moe_gb300 as kt
+import oracle as O
+from mxfp4_weight_moe_gb300 import synthetic as syn
+
+from helpers import OUT_RTOL, bf16_bits_np, bf16_to_f64, normwise_rel
+
+pytestmark = pytest.mark.gpu
+
+L, T, H, I, E, K = 3, 64, 256, 256, 8, 2
+
+
+def _layers():
+    weights, packs, logits = [], [], []
+    for l in range(L):
+        W = syn.make_weights(E, H, I, seed=100 + l, device="cpu")
+        weights.append(W)
+        packs.append(kt.Layerwise.pack(*W))
+        logits.append(syn.make_logits(T, E, "zipf", seed=l, device="cuda"))
+    return weights, packs, logits
+
+
+def test_layerwise_matches_sequential_and_serialized():
+    weights, packs, logits = _layers()
+    hidden = syn.make_hidden(T, H, 0, device="cuda")
+    lw = kt.Layerwise(packs, H, I, E, K, T_max=T)
+    try:
+        streamed = lw.prefill(hidden, logits)
+        serial = lw.prefill(hidden, logits, serialized=True)
+        torch.cuda.synchronize()
+    finally:
+        lw.close()
+    h = hidden
+    for l in range(L):
+        ids, w, *_ = kt.route_permute(logits[l], K)
+        h = kt.forward(h, ids, w, *[t.cuda() for t in weights[l]])
+    torch.cuda.synchronize()
+    assert torch.equal(streamed.view(torch.int16), h.view(torch.int16))
+    assert torch.equal(serial.view(torch.int16), h.view(torch.int16))
+    # the oracle chain on its own outputs
+    hb = bf16_bits_np(hidden)
+    for l in range(L):
+        ids, w = O.route(logits[l].cpu().numpy(), K)
+        hb = O.moe_forward(hb, ids, w, *[t.numpy() for t in weights[l]])["out"]
+    rel = normwise_rel(bf16_to_f64(bf16_bits_np(streamed)), bf16_to_f64(hb))
+    assert rel.max() <= OUT_RTOL * L, rel.max()
+
+
+def test_layerwise_copy_failure_is_reported_and_recoverable():
+    weights, packs, logits = _layers()
+    hidden = syn.make_hidden(T, H, 0, device="cuda")
+    lw = kt.Layerwise(packs, H, I, E, K, T_max=T)
+    try:
+        lw.inject_copy_failure(1)
+        with pytest.raises(kt.KTError) as ei:
+            lw.prefill(hidden, logits)
+        assert ei.value.status == -4
+        lw.inject_copy_failure(-1)
+        again = lw.prefill(hidden, logits)
+        ref = lw.prefill(hidden, logits, serialized=True)
+        torch.cuda.synchronize()
+        assert torch.equal(again.view(torch.int16), ref.view(torch.int16))
+    finally:
+        lw.close()
