@@ -214,6 +214,18 @@ uint64_t kt_moe_kernel_launches(void);
 kt_status kt_moe_profile_enable(int enable);
 kt_status kt_moe_profile_read(double* stage_ms, int* calls);
 
+/*
+ * Test hook for the device-side failure path.  wait_limit_us bounds every
+ * barrier wait inside the GEMM kernels (0 restores the default of 2 s).
+ * flags = KT_DEBUG_WITHHOLD_STAGE makes each GEMM CTA's producer withhold
+ * the first pipeline stage of its first tile (nothing is loaded into it and
+ * it is never signalled), so the MMA issuer's wait runs out: the kernel
+ * records KT_DEVERR_TIMEOUT_* in the error word, frees its tensor memory
+ * and returns; the CUDA context stays usable.  Process-wide; 0 disables.
+ */
+#define KT_DEBUG_WITHHOLD_STAGE 0x1
+kt_status kt_moe_debug_configure(uint64_t wait_limit_us, int flags);
+
 /* ------------------------------------------------------------------ */
 /* Layerwise prefill: stream layer l+1's experts host -> device while  */
 /* layer l computes (issue 2172, Background / motivation).             */

@@ -72,7 +72,10 @@ _SIGNATURES = {
     "kt_moe_kernel_launches": ([], ctypes.c_uint64),
     "kt_moe_profile_enable": ([_I], _I),
     "kt_moe_profile_read": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)], _I),
+    "kt_moe_debug_configure": ([ctypes.c_uint64, _I], _I),
 }
+
+KT_DEBUG_WITHHOLD_STAGE = 0x1
 
 STAGES = ("route", "permute", "quant", "fc1", "fc2", "combine")
 
@@ -239,6 +242,12 @@ def kernel_launches() -> int:
 def profile_enable(enable: bool = True):
     """Start (or stop) recording per-stage CUDA events; discards old records."""
     _check(lib().kt_moe_profile_enable(int(bool(enable))), "kt_moe_profile_enable")
+
+
+def debug_configure(wait_limit_us: int = 0, flags: int = 0):
+    """Test hook: bound the GEMM barrier waits and optionally withhold a stage
+    (see kt_moe_debug_configure); debug_configure() restores the defaults."""
+    _check(lib().kt_moe_debug_configure(int(wait_limit_us), int(flags)), "kt_moe_debug_configure")
 
 
 def profile_read() -> dict:

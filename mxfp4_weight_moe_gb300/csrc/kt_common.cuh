@@ -12,8 +12,8 @@
 
 namespace kt {
 
-// Longest any single barrier wait may take before the kernel gives up,
-// records the failing role in the device error word and returns.
+// Default longest any single barrier wait may take before the kernel gives
+// up, records the failing role in the device error word and returns.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -62,14 +62,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for the phase with parity `parity` to complete.  Returns false when
 // the deadline passes or another role of the CTA raised *abort_flag; the
 // barrier's state is then left as is and the caller must wind down.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     uint32_t it = 0;
     while (!mbar_try_wait(bar, parity)) {
         if ((++it & 15u) == 0u) {
             if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
         }
     }
     return true;

@@ -17,10 +17,12 @@
 // so SwiGLU needs only the accumulator tile.
 //
 // Warp roles (192 threads, one CTA per SM, persistent over tiles):
-//   warp 0     producer: TMA loads of the fp4 weight tile (unpacked to one
-//              byte per element in shared memory by the 16U4_ALIGN16B tensor
-//              map type) and of the e4m3 token tile, 4-byte cp.async gathers
-//              of both scale-factor tiles into the 128x4 block layout
+//   warp 0     producer: TMA loads of the fp4 weight tile (unpacked by the
+//              16U4_ALIGN16B tensor map type: each 16-byte shared-memory
+//              chunk holds 8 bytes = 16 packed values, then an 8-byte gap the
+//              copy leaves untouched) and of the e4m3 token tile, 4-byte
+//              cp.async gathers of both scale-factor tiles into the 128x4
+//              block layout
 //   warp 1     one thread issues tcgen05.cp (scales -> tensor memory) and
 //              tcgen05.mma (4 per K step), commits to the pipeline barriers
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator (warp w reads lanes
@@ -39,6 +41,9 @@ namespace kt {
 constexpr int kStages = 4;
 constexpr int kBK = 128;                     // K elements per pipeline stage
 constexpr int kSmemA = 128 * kBK;            // 16 KB: 128 rows x 128 bytes (fp4 unpacked)
+// The unpacking TMA counts the packed global bytes as transaction bytes
+// (half the shared-memory footprint): 128 rows x 64 bytes per stage.
+constexpr int kTxA = 128 * kBK / 2;
 constexpr int kSmemB = kTileTokens * kBK;    // 32 KB: 256 rows x 128 bytes
 constexpr int kOffSFA = kSmemA + kSmemB;     // 512 B scale block for the 128 weight rows
 constexpr int kOffSFB = kOffSFA + 512;       // 2 x 512 B scale blocks for 256 token rows
@@ -69,6 +74,8 @@ struct KParams {
     const float* topk_w;
     float* raw_out;
     int* err;
+    uint64_t wait_limit_ns;
+    int debug_flags;
 };
 
 // Tile u -> (expert, feature tile, token chunk); token chunks of one
@@ -178,11 +185,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             decode_tile(p, u, ti);
             int rowA0, rowA1;
             weight_rows<MODE>(p, ti, rowA0, rowA1);
-            const uint32_t tx = static_cast<uint32_t>(kSmemA + ti.nmma * kBK);
+            const uint32_t tx = static_cast<uint32_t>(kTxA + ti.nmma * kBK);
             const int nsfb = (ti.nmma + 31) >> 5;
             for (int kb = 0; kb < nk; ++kb) {
-                ok = __all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag));
+                ok = __all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns));
                 if (!ok) break;
+                if ((p.debug_flags & KT_DEBUG_WITHHOLD_STAGE) && u == static_cast<int>(blockIdx.x) && kb == 0) {
+                    // test hook: leave this stage unfilled and unsignalled
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    continue;
+                }
                 fence_proxy_async_smem();
                 const uint32_t sA = s_base + stage * kStageBytes;
                 const uint32_t sB = sA + kSmemA;
@@ -229,11 +244,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 TileInfo ti;
                 decode_tile(p, u, ti);
                 issued = true;
-                ok = mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag);
+                ok = mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.wait_limit_ns);
                 if (!ok) break;
                 tc_fence_after();
                 for (int kb = 0; kb < nk; ++kb) {
-                    ok = mbar_wait(full_bar(stage), phase, abort_flag);
+                    ok = mbar_wait(full_bar(stage), phase, abort_flag, p.wait_limit_ns);
                     if (!ok) break;
                     fence_proxy_async_smem();
                     tc_fence_after();
@@ -267,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // every tcgen05 operation issued above completes before teardown
             if (issued) {
                 tc_commit(drain_bar);
-                mbar_wait(drain_bar, 0, abort_flag);
+                mbar_wait(drain_bar, 0, abort_flag, p.wait_limit_ns);
             }
         }
     } else {
@@ -281,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
             TileInfo ti;
             decode_tile(p, u, ti);
-            ok = __all_sync(0xffffffffu, mbar_wait(acc_full, acc_phase, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(acc_full, acc_phase, abort_flag, p.wait_limit_ns));
             if (!ok) break;
             tc_fence_after();
             for (int c0 = 0; c0 < ti.nvalid; c0 += 32) {
@@ -453,6 +468,9 @@ kt_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
     kp.topk_w = a.topk_w;
     kp.raw_out = a.raw_out;
     kp.err = a.err;
+    const DebugSettings dbg = debug_settings();
+    kp.wait_limit_ns = dbg.wait_limit_ns;
+    kp.debug_flags = dbg.flags;
     cudaError_t e;
     switch (a.mode) {
         case GemmEpilogue::Raw: e = launch_mode<0>(mw, ma, kp, s); break;

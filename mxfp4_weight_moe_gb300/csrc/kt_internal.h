@@ -77,6 +77,13 @@ struct GemmArgs {
     int* err;
 };
 
+// Test-hook settings (kt_moe_debug_configure), read at each GEMM launch.
+struct DebugSettings {
+    uint64_t wait_limit_ns;
+    int flags;
+};
+DebugSettings debug_settings();
+
 // Encodes the tensor maps and launches the persistent tcgen05 GEMM.
 // Returns KT_OK, KT_ERR_CUDA (launch / map encoding failure).
 kt_status launch_gemm(const GemmArgs& a, cudaStream_t s);

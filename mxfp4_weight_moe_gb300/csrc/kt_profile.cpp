@@ -10,6 +10,13 @@
 namespace kt {
 
 static std::atomic<uint64_t> g_launches{0};
+static std::atomic<uint64_t> g_wait_limit_ns{0};
+static std::atomic<int> g_debug_flags{0};
+
+DebugSettings debug_settings() {
+    const uint64_t lim = g_wait_limit_ns.load();
+    return {lim ? lim : 2000000000ull, g_debug_flags.load()};
+}
 
 void count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 
@@ -53,6 +60,13 @@ StageTimer::~StageTimer() {
 extern "C" {
 
 uint64_t kt_moe_kernel_launches(void) { return kt::g_launches.load(); }
+
+kt_status kt_moe_debug_configure(uint64_t wait_limit_us, int flags) {
+    if (flags & ~KT_DEBUG_WITHHOLD_STAGE) return KT_ERR_INVALID_ARG;
+    kt::g_wait_limit_ns.store(wait_limit_us * 1000ull);
+    kt::g_debug_flags.store(flags);
+    return KT_OK;
+}
 
 kt_status kt_moe_profile_enable(int enable) {
     kt::g_prof_on = enable != 0;

@@ -172,3 +172,9 @@ def test_ops_reject_cpu_tensors():
         kt.forward(x, torch.zeros(2, 1, dtype=torch.int32), torch.zeros(2, 1), torch.zeros(1, 512, 128, dtype=torch.uint8),
                    torch.zeros(1, 512, 8, dtype=torch.uint8), torch.zeros(1, 256, 128, dtype=torch.uint8),
                    torch.zeros(1, 256, 8, dtype=torch.uint8))
+
+
+def test_debug_configure_rejects_unknown_flags():
+    with pytest.raises(kt.KTError):
+        kt.debug_configure(0, 0x80)
+    kt.debug_configure()

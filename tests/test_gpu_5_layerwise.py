@@ -2,10 +2,14 @@
 
 The streamed result must be bit-identical to calling route + forward layer
 by layer with device-resident weights, and to the serialized control
-("upload all experts -> compute -> synchronise" per layer); a short chain is
-also compared with the oracle run layer by layer on its own outputs.  A copy
-failure injected on the host must drain both streams and surface as an
-error, leaving the context usable.
+("upload all experts -> compute -> synchronise" per layer).  Each of those
+per-layer forwards is the oracle-checked path; a one-layer streamed prefill
+on generator inputs is compared with the oracle directly.  (A multi-layer
+chain is not compared with an oracle chain: the two chains' inputs diverge
+after layer 0 by bf16 rounding, and MXFP8 requantisation turns that into
+code flips, so the gap grows with depth for reasons unrelated to either
+implementation.)  A copy failure injected on the host must drain both
+streams and surface as an error, leaving the context usable.
 """
 import numpy as np
 import pytest
@@ -49,13 +53,21 @@ def test_layerwise_matches_sequential_and_serialized():
     torch.cuda.synchronize()
     assert torch.equal(streamed.view(torch.int16), h.view(torch.int16))
     assert torch.equal(serial.view(torch.int16), h.view(torch.int16))
-    # the oracle chain on its own outputs
-    hb = bf16_bits_np(hidden)
-    for l in range(L):
-        ids, w = O.route(logits[l].cpu().numpy(), K)
-        hb = O.moe_forward(hb, ids, w, *[t.numpy() for t in weights[l]])["out"]
-    rel = normwise_rel(bf16_to_f64(bf16_bits_np(streamed)), bf16_to_f64(hb))
-    assert rel.max() <= OUT_RTOL * L, rel.max()
+
+
+def test_layerwise_single_layer_matches_oracle():
+    weights, packs, logits = _layers()
+    hidden = syn.make_hidden(T, H, 0, device="cuda")
+    lw = kt.Layerwise(packs[:1], H, I, E, K, T_max=T)
+    try:
+        out = lw.prefill(hidden, logits[:1])
+        torch.cuda.synchronize()
+    finally:
+        lw.close()
+    ids, w = O.route(logits[0].cpu().numpy(), K)
+    ref = O.moe_forward(bf16_bits_np(hidden), ids, w, *[t.numpy() for t in weights[0]], want=("out_f64",))
+    rel = normwise_rel(bf16_to_f64(bf16_bits_np(out)), ref["out_f64"])
+    assert rel.max() <= OUT_RTOL, rel.max()
 
 
 def test_layerwise_copy_failure_is_reported_and_recoverable():
