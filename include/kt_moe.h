@@ -107,6 +107,39 @@ kt_status kt_moe_route_permute(const float* logits, int T, int E, int k, int ren
                                int32_t* perm, int32_t* inv_perm,
                                void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * Routing + permutation for callers that cannot allocate device memory.
+ *
+ * No counterpart on the pages: this is a convenience of this library.  Some
+ * callers have no way to hand over a scratch workspace and must not call
+ * cudaMalloc themselves -- for instance a plugin whose host framework owns
+ * all device memory and gives the plugin no workspace, or a latency-bound
+ * serving loop where cudaMalloc's implicit device synchronisation is not
+ * acceptable.  This entry point computes exactly what kt_moe_route_permute
+ * computes (same kernels, same outputs), but its scratch lives in a
+ * file-scope device array of KT_NOALLOC_SCRATCH_BYTES inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ *   - Arguments, outputs, limits and errors as for kt_moe_route_permute,
+ *     without ws/ws_bytes.  Sizes whose scratch need
+ *     (kt_moe_route_workspace_bytes(T, E, k)) exceeds
+ *     KT_NOALLOC_SCRATCH_BYTES return KT_ERR_WORKSPACE before anything runs
+ *     (1 MiB covers, e.g., T = 8192 tokens with E = 896, k = 16).
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture on the device.
+ *   - All calls share the one array and leave their scratch in it; each call
+ *     clears the error word it uses and fully rewrites the rest before
+ *     reading it.  Calls that overlap on the GPU (other streams, other host
+ *     threads) race on the array: serialise them.
+ *   - kt_moe_read_device_error cannot see this array; the outputs are the
+ *     same as kt_moe_route_permute's, whose error word reports bad ids.
+ */
+#define KT_NOALLOC_SCRATCH_BYTES (1u << 20)
+kt_status kt_moe_route_permute_noalloc(const float* logits, int T, int E, int k, int renormalize,
+                                       int32_t* topk_ids, float* topk_w, int32_t* expert_offsets,
+                                       int32_t* perm, int32_t* inv_perm, void* stream);
+
 /* ------------------------------------------------------------------ */
 /* The fused layer forward (quant, FC1 + SwiGLU + requant, FC2 +      */
 /* combine; it re-derives the permutation from topk_ids).             */

@@ -24,7 +24,7 @@ from . import build_ext
 __all__ = [
     "KTError", "lib", "route_permute", "forward", "workspace_bytes", "workspace_layout", "read_device_error",
     "grouped_gemm_f32", "Layerwise", "status_string", "check_fc_shapes", "kernel_launches", "profile_enable",
-    "profile_read", "STAGES",
+    "profile_read", "STAGES", "route_permute_noalloc",
 ]
 
 KT_OK = 0
@@ -73,7 +73,10 @@ _SIGNATURES = {
     "kt_moe_profile_enable": ([_I], _I),
     "kt_moe_profile_read": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)], _I),
     "kt_moe_debug_configure": ([ctypes.c_uint64, _I], _I),
+    "kt_moe_route_permute_noalloc": ([_VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP], _I),
 }
+
+KT_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 KT_DEBUG_WITHHOLD_STAGE = 0x1
 
@@ -144,6 +147,25 @@ def check_fc_shapes(w13: torch.Tensor, w2: torch.Tensor):
         raise ValueError(f"gated FC1 inter size {fc1_inter} must be twice the FC2 inter size {fc2_inter} "
                          f"(expected {2 * fc2_inter})")
     return E, fc2_inter, H
+
+
+def route_permute_noalloc(logits: torch.Tensor, k: int, renormalize: bool = True, stream=None, out=None):
+    """route_permute without a caller workspace: the scratch is a fixed device
+    array inside the library (for callers that cannot allocate device memory;
+    concurrent calls on different streams race on it).  Outputs as route_permute."""
+    _need(logits, "logits", torch.float32, 2)
+    T, E = logits.shape
+    dev = logits.device
+    if out is None:
+        out = (torch.empty(T, k, dtype=torch.int32, device=dev), torch.empty(T, k, dtype=torch.float32, device=dev),
+               torch.empty(E + 1, dtype=torch.int32, device=dev), torch.empty(T * k, dtype=torch.int32, device=dev),
+               torch.empty(T * k, dtype=torch.int32, device=dev))
+    ids, w, offsets, perm, inv = out
+    with torch.cuda.device(dev):
+        _check(lib().kt_moe_route_permute_noalloc(_ptr(logits), T, E, k, int(bool(renormalize)), _ptr(ids), _ptr(w),
+                                                  _ptr(offsets), _ptr(perm), _ptr(inv), _stream_ptr(stream, dev)),
+               "kt_moe_route_permute_noalloc")
+    return ids, w, offsets, perm, inv
 
 
 def workspace_bytes(T: int, H: int, I: int, E: int, k: int) -> int:

@@ -22,6 +22,11 @@ static kt_status fail(kt_status st, const char* fmt, ...) {
     return st;
 }
 
+kt_status report(kt_status st, const char* msg) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
+    return st;
+}
+
 kt_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return KT_OK;
     snprintf(g_last_error, sizeof(g_last_error), "CUDA error %d: %s", static_cast<int>(e), cudaGetErrorString(e));

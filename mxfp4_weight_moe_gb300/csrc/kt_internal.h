@@ -93,6 +93,8 @@ int sm_count();
 
 // Status helper: map a CUDA error to KT_ERR_CUDA, remembering the last one.
 kt_status cuda_status(cudaError_t e);
+// Record `msg` as this thread's kt_last_error() text and return `st`.
+kt_status report(kt_status st, const char* msg);
 
 // Measurement hooks (kt_profile.cpp): launch counter and, when profiling is
 // enabled, CUDA events recorded on the stream around one stage (RAII).
