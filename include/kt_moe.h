@@ -184,8 +184,12 @@ kt_status kt_mxfp4_moe_forward(const uint16_t* hidden, int T, int H,
  *   expert_offsets i32 [E+1]      chunk_prefix i32 [E+1] (token chunks per expert)
  *   perm, inv_perm i32 [S]        S = T*k
  *   hist           i32 [tiles*E]  permutation scratch
- *   a1 e4m3 [S, H], a1_sf e8m0 [S, H/32]   (rows in permuted order)
- *   a2 e4m3 [S, I], a2_sf e8m0 [S, I/32]   (rows in permuted order)
+ *   a1 e4m3 [S, H]  (rows in permuted order)
+ *   a1_sf           A1's e8m0 scales, K-step-major: u32 [H/128][S4] with
+ *                   S4 = S rounded up to a multiple of 4; word (ks, p) holds
+ *                   row p's scale bytes for 32-blocks 4ks..4ks+3 (block b in
+ *                   byte b % 4)
+ *   a2 e4m3 [S, I], a2_sf likewise u32 [I/128][S4] (rows in permuted order)
  *   y  bf16 [S, H]  topk_w-weighted FC2 output, rows in slot order
  */
 typedef struct kt_ws_layout {
@@ -210,10 +214,10 @@ kt_status kt_moe_read_device_error(const void* ws, int* code, void* stream);
  *   w       fp4x2 [E, N, K/2] + w_sf e8m0 [E, N, K/32]
  *   out     f32 [S, N]: out[p, n] = sum_K act[p] * w[e(p), n] (block-scaled);
  *           rows outside [expert_offsets[0], expert_offsets[E]) untouched
- *   ws      >= kt_mx_gemm_workspace_bytes(E) bytes
+ *   ws      >= kt_mx_gemm_workspace_bytes(S, K, E) bytes
  * Limits: K % 128 == 0, N % 128 == 0, E <= 1024.
  */
-size_t kt_mx_gemm_workspace_bytes(int E);
+size_t kt_mx_gemm_workspace_bytes(int S, int K, int E);
 kt_status kt_mx_grouped_gemm_f32(const uint8_t* act, const uint8_t* act_sf, int S, int K,
                                  const int32_t* expert_offsets,
                                  const uint8_t* w, const uint8_t* w_sf, int E, int N,

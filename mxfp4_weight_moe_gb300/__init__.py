@@ -60,7 +60,7 @@ _SIGNATURES = {
     "kt_mxfp4_moe_forward": ([_VP, _I, _I, _VP, _VP, _I, _VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _SZ, _VP], _I),
     "kt_moe_workspace_layout": ([_I, _I, _I, _I, _I, ctypes.POINTER(WsLayout)], _I),
     "kt_moe_read_device_error": ([_VP, ctypes.POINTER(_I), _VP], _I),
-    "kt_mx_gemm_workspace_bytes": ([_I], _SZ),
+    "kt_mx_gemm_workspace_bytes": ([_I, _I, _I], _SZ),
     "kt_mx_grouped_gemm_f32": ([_VP, _VP, _I, _I, _VP, _VP, _VP, _I, _I, _VP, _VP, _SZ, _VP], _I),
     "kt_layerwise_pack_bytes": ([_I, _I, _I], _SZ),
     "kt_layerwise_pack_offsets": ([_I, _I, _I, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ), ctypes.POINTER(_SZ),
@@ -172,6 +172,14 @@ def workspace_bytes(T: int, H: int, I: int, E: int, k: int) -> int:
     return int(lib().kt_moe_workspace_bytes(T, H, I, E, k))
 
 
+def scales_from_kstep_major(words: torch.Tensor, S: int, K: int) -> torch.Tensor:
+    """Plain [S, K/32] e8m0 bytes from a workspace's K-step-major scale region
+    (u32 [K/128][S4], byte b % 4 of word (b // 4, row) is block b)."""
+    S4 = (S + 3) // 4 * 4
+    w = words[: (K // 128) * S4 * 4].view(K // 128, S4, 4)
+    return w[:, :S, :].permute(1, 0, 2).reshape(S, K // 32)
+
+
 def workspace_layout(T: int, H: int, I: int, E: int, k: int) -> dict:
     L = WsLayout()
     _check(lib().kt_moe_workspace_layout(T, H, I, E, k, ctypes.byref(L)), "kt_moe_workspace_layout")
@@ -248,7 +256,7 @@ def grouped_gemm_f32(act, act_sf, expert_offsets, w, w_sf, out=None, stream=None
     E, N, _ = w.shape
     if out is None:
         out = torch.zeros(S, N, dtype=torch.float32, device=dev)
-    ws = torch.empty(max(int(lib().kt_mx_gemm_workspace_bytes(E)), 1), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(int(lib().kt_mx_gemm_workspace_bytes(S, K, E)), 1), dtype=torch.uint8, device=dev)
     with torch.cuda.device(dev):
         _check(lib().kt_mx_grouped_gemm_f32(_ptr(act), _ptr(act_sf), S, K, _ptr(expert_offsets), _ptr(w), _ptr(w_sf),
                                             E, N, _ptr(out), _ptr(ws), ws.numel(), _stream_ptr(stream, dev)),

@@ -62,10 +62,11 @@ bool ws_layout(int T, int H, int I, int E, int k, kt_ws_layout* L) {
     L->perm = take(sizeof(int32_t) * S);
     L->inv_perm = take(sizeof(int32_t) * S);
     L->hist = take(sizeof(int32_t) * static_cast<size_t>(perm_tiles(static_cast<long long>(S))) * E);
+    const size_t S4 = static_cast<size_t>(sf_rows(static_cast<long long>(S)));
     L->a1 = take(S * H);
-    L->a1_sf = take(S * (H / 32));
+    L->a1_sf = take(S4 * (H / 32));
     L->a2 = take(S * I);
-    L->a2_sf = take(S * (I / 32));
+    L->a2_sf = take(S4 * (I / 32));
     L->y = take(S * H * sizeof(uint16_t));
     L->total = off;
     return true;
@@ -224,7 +225,8 @@ kt_status kt_mxfp4_moe_forward(const uint16_t* hidden, int T, int H, const int32
     }
     {
         StageTimer timer(KT_STAGE_QUANT, s);
-        if ((st = cuda_status(launch_quant_scatter(hidden, T, H, k, inv_perm, a1, a1_sf, s))) != KT_OK) return st;
+        if ((st = cuda_status(launch_quant_scatter(hidden, T, H, k, inv_perm, a1, a1_sf, sf_rows(S), s))) != KT_OK)
+            return st;
     }
 
     GemmArgs fc1{};
@@ -290,9 +292,10 @@ kt_status kt_moe_read_device_error(const void* ws, int* code, void* stream) {
     return KT_OK;
 }
 
-size_t kt_mx_gemm_workspace_bytes(int E) {
-    if (E <= 0 || E > kMaxExperts) return 0;
-    return 1024 + align_up(sizeof(int32_t) * (E + 1), 1024);
+size_t kt_mx_gemm_workspace_bytes(int S, int K, int E) {
+    if (S < 0 || K <= 0 || K % 128 || E <= 0 || E > kMaxExperts) return 0;
+    return 1024 + align_up(sizeof(int32_t) * (E + 1), 1024) +
+           align_up(static_cast<size_t>(sf_rows(S)) * (K / 32), 1024);
 }
 
 kt_status kt_mx_grouped_gemm_f32(const uint8_t* act, const uint8_t* act_sf, int S, int K,
@@ -308,14 +311,16 @@ kt_status kt_mx_grouped_gemm_f32(const uint8_t* act, const uint8_t* act_sf, int 
     if (!aligned(act, 16) || !aligned(w, 32) || !aligned(act_sf, 4) || !aligned(w_sf, 4) || !aligned(out, 16))
         return fail(KT_ERR_ALIGNMENT, "misaligned pointer");
     if (!aligned(ws, 256)) return fail(KT_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-    if (ws_bytes < kt_mx_gemm_workspace_bytes(E)) return fail(KT_ERR_WORKSPACE, "workspace too small");
+    if (ws_bytes < kt_mx_gemm_workspace_bytes(S, K, E)) return fail(KT_ERR_WORKSPACE, "workspace too small");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* base = static_cast<uint8_t*>(ws);
     int* err = reinterpret_cast<int*>(base);
     int32_t* chunk_prefix = reinterpret_cast<int32_t*>(base + 1024);
+    uint8_t* sf_km = base + 1024 + align_up(sizeof(int32_t) * (E + 1), 1024);
     kt_status st;
     if ((st = cuda_status(cudaMemsetAsync(err, 0, sizeof(int), s))) != KT_OK) return st;
     if ((st = cuda_status(launch_chunk_prefix(expert_offsets, E, chunk_prefix, s))) != KT_OK) return st;
+    if ((st = cuda_status(launch_sf_to_kstep_major(act_sf, S, K, sf_km, sf_rows(S), s))) != KT_OK) return st;
     GemmArgs g{};
     g.mode = GemmEpilogue::Raw;
     g.expert_offsets = expert_offsets;
@@ -329,7 +334,7 @@ kt_status kt_mx_grouped_gemm_f32(const uint8_t* act, const uint8_t* act_sf, int 
     g.w = w;
     g.w_sf = w_sf;
     g.act = act;
-    g.act_sf = act_sf;
+    g.act_sf = sf_km;
     g.raw_out = out;
     g.err = err;
     return launch_gemm(g, s);

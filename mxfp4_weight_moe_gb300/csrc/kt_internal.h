@@ -11,9 +11,10 @@
 
 namespace kt {
 
-// Token rows of one GEMM tile (the MMA N extent, at most 256) and the number
-// of slots one permutation tile handles.
-constexpr int kTileTokens = 256;
+// Token rows of one GEMM tile (the MMA N extent; two accumulator buffers of
+// this many columns fit in tensor memory next to the scale columns) and the
+// number of slots one permutation tile handles.
+constexpr int kTileTokens = 224;
 constexpr int kPermTile = 1024;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
@@ -21,6 +22,12 @@ constexpr int kMaxTopK = 32;
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 inline int perm_tiles(long long S) { return static_cast<int>((S + kPermTile - 1) / kPermTile); }
+
+// Activation scales (A1, A2) are stored K-step-major: a u32 array
+// [K/128][S4] whose word (ks, p) holds the four e8m0 bytes of row p for the
+// 32-element blocks 4ks..4ks+3 (block b in byte b % 4).  S4 = S rounded up to
+// a multiple of 4 keeps every row of the array 16-byte aligned for TMA.
+inline int sf_rows(long long S) { return static_cast<int>((S + 3) / 4 * 4); }
 
 // Workspace carving (offsets relative to the 256-byte aligned base).
 bool ws_layout(int T, int H, int I, int E, int k, kt_ws_layout* L);
@@ -42,9 +49,12 @@ cudaError_t launch_permute(const int32_t* ids, long long S, int E, int32_t* hist
                            int32_t* chunk_prefix, int32_t* perm, int32_t* inv_perm, int* err, cudaStream_t s);
 // chunk_prefix [E+1] from expert_offsets alone (for the diagnostic GEMM).
 cudaError_t launch_chunk_prefix(const int32_t* expert_offsets, int E, int32_t* chunk_prefix, cudaStream_t s);
-// MXFP8 quantisation of hidden rows, each written to its k permuted rows.
+// MXFP8 quantisation of hidden rows, each written to its k permuted rows
+// (codes [S, H]; scales K-step-major with S4 = sf_rows(S)).
 cudaError_t launch_quant_scatter(const uint16_t* hidden, int T, int H, int k, const int32_t* inv_perm, uint8_t* a1,
-                                 uint8_t* a1_sf, cudaStream_t s);
+                                 uint8_t* a1_sf, int S4, cudaStream_t s);
+// Plain [S, K/32] scale bytes -> K-step-major layout (diagnostic GEMM entry).
+cudaError_t launch_sf_to_kstep_major(const uint8_t* plain, int S, int K, uint8_t* out, int S4, cudaStream_t s);
 // out[t] = sum over valid slots of y[t*k + j] (y already weighted).
 cudaError_t launch_combine(const uint16_t* y, const int32_t* ids, int T, int H, int k, int E, uint16_t* out,
                            cudaStream_t s);
@@ -63,8 +73,8 @@ struct GemmArgs {
     const uint8_t* w;      // fp4x2 [E, rows_w, K/2]
     const uint8_t* w_sf;   // e8m0  [E, rows_w, K/32]
     const uint8_t* act;    // e4m3  [S, K]
-    const uint8_t* act_sf; // e8m0  [S, K/32]
-    // SwiGLU outputs: A2 e4m3 [S, I] + e8m0 [S, I/32]
+    const uint8_t* act_sf; // e8m0, K-step-major u32 [K/128][sf_rows(S)]
+    // SwiGLU outputs: A2 e4m3 [S, I] + e8m0 K-step-major [I/128][sf_rows(S)]
     uint8_t* a2;
     uint8_t* a2_sf;
     // Combine outputs: y bf16 [S, H] in slot order, scaled by topk_w

@@ -16,7 +16,8 @@ namespace kt {
 // every permuted row the token's k slots map to.
 __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __restrict__ hidden, int T, int H, int k,
                                                             const int32_t* __restrict__ inv_perm,
-                                                            uint8_t* __restrict__ a1, uint8_t* __restrict__ a1_sf) {
+                                                            uint8_t* __restrict__ a1, uint8_t* __restrict__ a1_sf,
+                                                            int S4) {
     __shared__ int s_dst[8][kMaxTopK];
     const int wib = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -62,15 +63,46 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
             uint4* dst = reinterpret_cast<uint4*>(a1 + static_cast<size_t>(p) * H + b * 32);
             dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
             dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-            a1_sf[static_cast<size_t>(p) * nblk + b] = sbyte;
+            a1_sf[((static_cast<size_t>(b >> 2) * S4 + p) << 2) + (b & 3)] = sbyte;
         }
     }
 }
 
 cudaError_t launch_quant_scatter(const uint16_t* hidden, int T, int H, int k, const int32_t* inv_perm, uint8_t* a1,
-                                 uint8_t* a1_sf, cudaStream_t s) {
+                                 uint8_t* a1_sf, int S4, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    quant_scatter_kernel<<<(T + 7) / 8, 256, 0, s>>>(hidden, T, H, k, inv_perm, a1, a1_sf);
+    quant_scatter_kernel<<<(T + 7) / 8, 256, 0, s>>>(hidden, T, H, k, inv_perm, a1, a1_sf, S4);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// Plain [S, K/32] scale bytes -> K-step-major u32 [K/128][S4] (one thread per
+// row and K step; rows S..S4-1 are zero).
+__global__ void __launch_bounds__(256) sf_to_kstep_major_kernel(const uint8_t* __restrict__ plain, int S, int K,
+                                                                uint32_t* __restrict__ out, int S4) {
+    const int nks = K / 128;
+    const long long n = static_cast<long long>(nks) * S4;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int ks = static_cast<int>(i / S4);
+        const int r = static_cast<int>(i % S4);
+        uint32_t v = 0;
+        if (r < S) {
+            const uint8_t* src = plain + static_cast<size_t>(r) * (K / 32) + ks * 4;
+            v = static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 8) |
+                (static_cast<uint32_t>(src[2]) << 16) | (static_cast<uint32_t>(src[3]) << 24);
+        }
+        out[i] = v;
+    }
+}
+
+cudaError_t launch_sf_to_kstep_major(const uint8_t* plain, int S, int K, uint8_t* out, int S4, cudaStream_t s) {
+    const long long n = static_cast<long long>(K / 128) * S4;
+    if (n <= 0) return cudaSuccess;
+    long long blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    sf_to_kstep_major_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(plain, S, K, reinterpret_cast<uint32_t*>(out),
+                                                                      S4);
     count_launches(1);
     return cudaGetLastError();
 }

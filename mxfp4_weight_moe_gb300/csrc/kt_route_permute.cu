@@ -187,42 +187,55 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ h
     for (long long p = total_cnt + threadIdx.x; p < S; p += blockDim.x) perm[p] = -1;
 }
 
-// Pass 3 (one warp per tile): stable ranks inside the tile by a warp-serial
-// sweep in slot order; the peers of a slot in one 32-slot round are found
-// with match.any, so equal experts keep their slot order.
-__global__ void __launch_bounds__(32) perm_scatter_kernel(const int32_t* __restrict__ ids, long long S, int E,
-                                                          const int32_t* __restrict__ tile_base,
-                                                          const int32_t* __restrict__ offsets,
-                                                          int32_t* __restrict__ perm,
-                                                          int32_t* __restrict__ inv_perm) {
-    extern __shared__ int sh_run[];
-    const int lane = threadIdx.x;
-    for (int e = lane; e < E; e += 32) sh_run[e] = 0;
-    __syncwarp();
+// Pass 3 (one block of 128 threads per tile): the tile's ids and the
+// per-expert bases (expert offset + tile prefix) are staged in shared memory
+// first; then one warp sweeps the tile in slot order, 32 slots per round,
+// finding the peers of each slot with match.any so that equal experts keep
+// their slot order.  Ranks and outputs are written back by all 128 threads.
+__global__ void __launch_bounds__(128) perm_scatter_kernel(const int32_t* __restrict__ ids, long long S, int E,
+                                                           const int32_t* __restrict__ tile_base,
+                                                           const int32_t* __restrict__ offsets,
+                                                           int32_t* __restrict__ perm,
+                                                           int32_t* __restrict__ inv_perm) {
+    extern __shared__ int sh[];
+    int* s_base = sh;                      // [E]   offsets[e] + tile prefix, then running count
+    int* s_id = sh + E;                    // [kPermTile] expert of each slot (-1 invalid / past S)
+    int* s_pos = s_id + kPermTile;         // [kPermTile] permuted row of each slot
     const long long base = static_cast<long long>(blockIdx.x) * kPermTile;
     const int32_t* tb = tile_base + static_cast<size_t>(blockIdx.x) * E;
-    for (int r = 0; r < kPermTile / 32; ++r) {
-        const long long s = base + r * 32 + lane;
-        if (base + r * 32 >= S) break;   // warp-uniform
-        const int e = (s < S) ? ids[s] : -1;
-        const bool valid = (s < S) && e >= 0 && e < E;
-        const int key = valid ? e : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, key);
-        const int rank = __popc(peers & ((1u << lane) - 1u));
-        const int leader = __ffs(peers) - 1;
-        const int before = valid ? sh_run[e] : 0;
-        __syncwarp();
-        if (valid && lane == leader) sh_run[e] = before + __popc(peers);
-        __syncwarp();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_base[e] = offsets[e] + tb[e];
+    for (int i = threadIdx.x; i < kPermTile; i += blockDim.x) {
+        const long long s = base + i;
+        int e = -1;
         if (s < S) {
-            if (valid) {
-                const int p = offsets[e] + tb[e] + before + rank;
-                perm[p] = static_cast<int32_t>(s);
-                inv_perm[s] = p;
-            } else {
-                inv_perm[s] = -1;
-            }
+            e = ids[s];
+            if (e < 0 || e >= E) e = -1;
         }
+        s_id[i] = e;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        for (int r = 0; r < kPermTile / 32; ++r) {
+            if (base + r * 32 >= S) break;   // warp-uniform
+            const int e = s_id[r * 32 + lane];
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            const int leader = __ffs(peers) - 1;
+            const int before = (e >= 0) ? s_base[e] : 0;
+            __syncwarp();
+            if (e >= 0 && lane == leader) s_base[e] = before + __popc(peers);
+            __syncwarp();
+            s_pos[r * 32 + lane] = (e >= 0) ? before + rank : -1;
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kPermTile; i += blockDim.x) {
+        const long long s = base + i;
+        if (s >= S) break;
+        const int pos = s_pos[i];
+        inv_perm[s] = pos;
+        if (pos >= 0) perm[pos] = static_cast<int32_t>(s);
     }
 }
 
@@ -240,7 +253,8 @@ cudaError_t launch_permute(const int32_t* ids, long long S, int E, int32_t* hist
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (ntiles > 0) {
-        perm_scatter_kernel<<<ntiles, 32, E * sizeof(int), s>>>(ids, S, E, hist, expert_offsets, perm, inv_perm);
+        perm_scatter_kernel<<<ntiles, 128, (E + 2 * kPermTile) * sizeof(int), s>>>(ids, S, E, hist, expert_offsets,
+                                                                                     perm, inv_perm);
         count_launches(1);
         e = cudaGetLastError();
     }

@@ -121,7 +121,19 @@ def test_grouped_gemm_checks():
     assert L.kt_mx_grouped_gemm_f32(v(P), v(P), 10, 128, v(P), v(P + 16), v(P), 2, 128, v(P), v(P), 1 << 20,
                                     None) == ALIGN
     assert L.kt_mx_grouped_gemm_f32(v(P), v(P), 10, 128, v(P), v(P), v(P), 2, 128, v(P), v(P), 8, None) == WS
+    assert L.kt_mx_gemm_workspace_bytes(10, 128, 2) > 1024
     assert L.kt_mx_grouped_gemm_f32(v(P), v(P), 0, 128, None, None, None, 2, 128, None, None, 0, None) == KT_OK
+
+
+def test_kstep_major_scale_view_roundtrip():
+    S, K = 7, 512
+    plain = torch.randint(0, 255, (S, K // 32), dtype=torch.uint8)
+    S4 = 8
+    words = torch.zeros(K // 128, S4, 4, dtype=torch.uint8)
+    for r in range(S):
+        for b in range(K // 32):
+            words[b // 4, r, b % 4] = plain[r, b]
+    assert torch.equal(kt.scales_from_kstep_major(words.reshape(-1), S, K), plain)
 
 
 def test_workspace_layout_is_ordered_and_aligned():

@@ -59,7 +59,7 @@ def _check_case(hidden, ids_np, w_np, W, tokens=None, check_a=True):
     # A1 (bit-exact) on the rows of the checked tokens
     if check_a:
         a1 = ws_view(ws, lay["a1"], S * H).reshape(S, H)
-        a1_sf = ws_view(ws, lay["a1_sf"], S * H // 32).reshape(S, H // 32)
+        a1_sf = kt.scales_from_kstep_major(ws[lay["a1_sf"]:], S, H).cpu().numpy()
         rc, rs = O.quant_rows_bf16(hbits[tokens])
         for i, t in enumerate(tokens):
             for j in range(k):
@@ -72,7 +72,7 @@ def _check_case(hidden, ids_np, w_np, W, tokens=None, check_a=True):
     # A2: codes at the permuted rows of the checked slots
     if check_a:
         a2 = ws_view(ws, lay["a2"], S * I).reshape(S, I)
-        a2_sf = ws_view(ws, lay["a2_sf"], S * I // 32).reshape(S, I // 32)
+        a2_sf = kt.scales_from_kstep_major(ws[lay["a2_sf"]:], S, I).cpu().numpy()
         gc, gs, rc2, rs2 = [], [], [], []
         for i, t in enumerate(tokens):
             for j in range(k):
