@@ -184,12 +184,15 @@ kt_status kt_mxfp4_moe_forward(const uint16_t* hidden, int T, int H,
  *   expert_offsets i32 [E+1]      chunk_prefix i32 [E+1] (token chunks per expert)
  *   perm, inv_perm i32 [S]        S = T*k
  *   hist           i32 [tiles*E]  permutation scratch
- *   a1 e4m3 [S, H]  (rows in permuted order)
+ *   a1 e4m3 [S, H]  (rows in permuted order; the buffer has room for S
+ *                   rounded up to a multiple of 8 rows, the GEMM reads
+ *                   token rows in groups of 8 and discards the padding)
  *   a1_sf           A1's e8m0 scales, K-step-major: u32 [H/128][S4] with
  *                   S4 = S rounded up to a multiple of 4; word (ks, p) holds
  *                   row p's scale bytes for 32-blocks 4ks..4ks+3 (block b in
  *                   byte b % 4)
- *   a2 e4m3 [S, I], a2_sf likewise u32 [I/128][S4] (rows in permuted order)
+ *   a2 e4m3 [S, I] (padded like a1), a2_sf likewise u32 [I/128][S4]
+ *                   (rows in permuted order)
  *   y  bf16 [S, H]  topk_w-weighted FC2 output, rows in slot order
  */
 typedef struct kt_ws_layout {
@@ -214,7 +217,9 @@ kt_status kt_moe_read_device_error(const void* ws, int* code, void* stream);
  *   w       fp4x2 [E, N, K/2] + w_sf e8m0 [E, N, K/32]
  *   out     f32 [S, N]: out[p, n] = sum_K act[p] * w[e(p), n] (block-scaled);
  *           rows outside [expert_offsets[0], expert_offsets[E]) untouched
- *   ws      >= kt_mx_gemm_workspace_bytes(S, K, E) bytes
+ *   ws      >= kt_mx_gemm_workspace_bytes(S, K, E) bytes (holds the chunk
+ *           prefix, the scales in K-step-major order and a copy of act padded
+ *           to a multiple of 8 rows)
  * Limits: K % 128 == 0, N % 128 == 0, E <= 1024.
  */
 size_t kt_mx_gemm_workspace_bytes(int S, int K, int E);

@@ -63,9 +63,10 @@ bool ws_layout(int T, int H, int I, int E, int k, kt_ws_layout* L) {
     L->inv_perm = take(sizeof(int32_t) * S);
     L->hist = take(sizeof(int32_t) * static_cast<size_t>(perm_tiles(static_cast<long long>(S))) * E);
     const size_t S4 = static_cast<size_t>(sf_rows(static_cast<long long>(S)));
-    L->a1 = take(S * H);
+    const size_t S8 = static_cast<size_t>(act_rows(static_cast<long long>(S)));
+    L->a1 = take(S8 * H);
     L->a1_sf = take(S4 * (H / 32));
-    L->a2 = take(S * I);
+    L->a2 = take(S8 * I);
     L->a2_sf = take(S4 * (I / 32));
     L->y = take(S * H * sizeof(uint16_t));
     L->total = off;
@@ -292,10 +293,12 @@ kt_status kt_moe_read_device_error(const void* ws, int* code, void* stream) {
     return KT_OK;
 }
 
+// error word | chunk prefix [E+1] | K-step-major scales | activation codes padded to act_rows(S) rows
 size_t kt_mx_gemm_workspace_bytes(int S, int K, int E) {
     if (S < 0 || K <= 0 || K % 128 || E <= 0 || E > kMaxExperts) return 0;
     return 1024 + align_up(sizeof(int32_t) * (E + 1), 1024) +
-           align_up(static_cast<size_t>(sf_rows(S)) * (K / 32), 1024);
+           align_up(static_cast<size_t>(sf_rows(S)) * (K / 32), 1024) +
+           align_up(static_cast<size_t>(act_rows(S)) * K, 1024);
 }
 
 kt_status kt_mx_grouped_gemm_f32(const uint8_t* act, const uint8_t* act_sf, int S, int K,
@@ -317,8 +320,12 @@ kt_status kt_mx_grouped_gemm_f32(const uint8_t* act, const uint8_t* act_sf, int 
     int* err = reinterpret_cast<int*>(base);
     int32_t* chunk_prefix = reinterpret_cast<int32_t*>(base + 1024);
     uint8_t* sf_km = base + 1024 + align_up(sizeof(int32_t) * (E + 1), 1024);
+    uint8_t* act_pad = sf_km + align_up(static_cast<size_t>(sf_rows(S)) * (K / 32), 1024);
     kt_status st;
     if ((st = cuda_status(cudaMemsetAsync(err, 0, sizeof(int), s))) != KT_OK) return st;
+    if ((st = cuda_status(cudaMemcpyAsync(act_pad, act, static_cast<size_t>(S) * K, cudaMemcpyDeviceToDevice, s))) !=
+        KT_OK)
+        return st;
     if ((st = cuda_status(launch_chunk_prefix(expert_offsets, E, chunk_prefix, s))) != KT_OK) return st;
     if ((st = cuda_status(launch_sf_to_kstep_major(act_sf, S, K, sf_km, sf_rows(S), s))) != KT_OK) return st;
     GemmArgs g{};
@@ -333,7 +340,7 @@ kt_status kt_mx_grouped_gemm_f32(const uint8_t* act, const uint8_t* act_sf, int 
     g.H = 0;
     g.w = w;
     g.w_sf = w_sf;
-    g.act = act;
+    g.act = act_pad;
     g.act_sf = sf_km;
     g.raw_out = out;
     g.err = err;

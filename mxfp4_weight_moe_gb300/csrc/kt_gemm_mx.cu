@@ -11,29 +11,54 @@
 // kernels the pages discuss.
 //
 // Tile = 128 weight rows (MMA M) x up to kTileTokens token rows of one expert
-// (MMA N, a multiple of 16), K streamed in steps of 128.  Weights sit on the
-// M side ("swap AB") so that experts with few tokens waste little MMA work.
-// For FC1 the 128 weight rows are 64 gate rows and the matching 64 up rows,
-// so SwiGLU needs only the accumulator tile.
+// (MMA N, a multiple of 16), K streamed in stages of 256 (tiles of at most
+// kSmallN token rows) or 128 (larger tiles, so that four stages fit in
+// flight).  Weights sit on the M side ("swap AB") so that experts with few
+// tokens waste little MMA work.  For FC1 the 128 weight rows are 64 gate rows
+// and the matching 64 up rows, so SwiGLU needs only the accumulator tile.  A
+// tile's token rows start at the expert's first row rounded down to a
+// multiple of 8 (up to 7 leading rows of the previous expert ride along and
+// are discarded), so that its token box decomposes into whole 8-row groups.
 //
-// Warp roles (224 threads, one CTA per SM, persistent over tiles):
-//   warp 0     TMA producer: one lane issues, per K step, one TMA for the
-//              whole fp4 weight tile (for FC1 a 3-D view of w13 puts the 64
-//              gate rows and the 64 matching up rows in one box; the
-//              16U4_ALIGN16B type unpacks it to one byte per element in
-//              shared memory: 8 data bytes then an 8-byte gap the copy leaves
-//              untouched, and counts the packed bytes as transaction bytes)
-//              and at most four boxes (128/64/32/16 rows) for the e4m3 token
-//              tile.
-//   warp 1     one thread issues tcgen05.cp (scales -> tensor memory) and
-//              tcgen05.mma (4 per K step) and commits to the barriers.
-//   warp 2     scale warp: per 4 K steps it TMA-loads the weight scales
-//              (16-byte rows of the plain [rows, K/32] layout) and the token
-//              scales (the K-step-major u32 layout the quantisers write) into
-//              a staging buffer, builds the 128x4 scale blocks the MMA reads,
-//              and prefetches the weight bytes of a later group of K steps
-//              into L2.
-//   warps 3-6  epilogue: tcgen05.ld of the accumulator (warp w reads lanes
+// Pipeline.  One stage is a weight tile of 128 rows x kqs*128 fp4 (one TMA
+// box; the 16U4_ALIGN16B type unpacks it to one byte per element in shared
+// memory and counts the packed bytes as transaction bytes) plus the token
+// tile of N rows x kqs*128 e4m3 bytes, kqs = 2 or 1 K-quads of 128.  Both sit
+// back to back in one ring of shared memory whose stages take only the bytes
+// they need.  Two producer threads share the ring bookkeeping: one loads
+// weight tiles, the other token tiles; both arrive on the stage's full
+// barrier.  On GB300 one thread that waits on a barrier, arrives on another
+// and issues a TMA manages about one stage per 250 ns, so the producer is
+// split and small-N stages carry 16 KB of packed weights.
+//
+// Clusters.  The CTAs of a cluster (cl = 1, 2 or 4) work on the same token
+// chunk with consecutive feature tiles.  Each loads 1/cl of the token rows
+// and multicasts them to all, so a token row leaves L2 once per cluster
+// instead of once per feature tile; each CTA's MMA commit releases the stage
+// in every CTA of the cluster (the empty barriers count cl arrivals).
+//
+// Shared-memory operand layouts (K-major, 128-byte swizzle):
+//   weights  [K quad q][128 rows][128 B]                 (rows 128 B apart)
+//   tokens   [8-row group g][K quad q][8 rows][128 B]    (groups kqs KB apart)
+// so the MMA descriptor of quad q starts at the quad's first row with 1024 B
+// (weights) or kqs * 1024 B (tokens) between 8-row groups.
+//
+// Warp roles (256 threads, one CTA per SM, persistent over tiles):
+//   warp 0     weight producer (one lane): one 3-D (FC1: 4-D) TMA box with
+//              the stage's K quads of the weight tile.
+//   warp 1     MMA issuer: the whole warp follows the pipeline, one elected
+//              lane issues tcgen05.cp (scales -> tensor memory) and
+//              tcgen05.mma (4 per K quad) and commits to the barriers.
+//   warp 2     scale warp: per group of 4 K-quads it TMA-loads the weight
+//              scales (16-byte rows of the plain [rows, K/32] layout) and the
+//              token scales (the K-step-major u32 layout the quantisers
+//              write) into a staging ring ahead of use, builds the 128x4
+//              scale blocks the MMA reads, and prefetches the weight bytes of
+//              a later group into L2.
+//   warp 3     token producer (one lane): one 4-D TMA box per stage with
+//              this CTA's share of the tile's token rows (a map per share
+//              size), multicast to the cluster.
+//   warps 4-7  epilogue: tcgen05.ld of the accumulator (warp w reads lanes
 //              32*(w%4)..+31), fused math, global stores.  Two accumulator
 //              buffers let one tile's epilogue overlap the next main loop.
 // Every barrier wait has a deadline; on expiry the role records itself in
@@ -47,39 +72,73 @@
 
 namespace kt {
 
-constexpr int kStages = 4;
-constexpr int kBK = 128;                      // K elements per pipeline stage
-constexpr int kSmemA = 128 * kBK;             // 16 KB: 128 rows x 128 bytes (fp4 unpacked)
-constexpr int kTxA = 128 * kBK / 2;           // the unpacking TMA counts packed bytes
-constexpr int kSmemB = kTileTokens * kBK;     // 28 KB: up to 224 token rows x 128 bytes
-constexpr int kStageBytes = kSmemA + kSmemB;  // 44 KB
-constexpr int kGroup = 4;                     // K steps per scale group
-constexpr int kSfStep = 512 + 1024;           // per K step: weight block + up to 2 token blocks
-constexpr int kSfBytes = kGroup * kSfStep;    // one scale-block buffer (two of them)
+constexpr int kQuadW = 128 * 128;             // one K quad of the weight tile in shared memory (fp4 unpacked)
+constexpr uint32_t kQuadWTx = 128 * 128 / 2;  // ... and its transaction bytes (the unpacking TMA counts packed bytes)
+// Build-time tuning: the largest tile (token rows) that uses two-quad stages,
+// and the largest cluster the launcher may pick.  Measured on GB300 (FC1+FC2
+// of the DSV4-shaped, Kimi-K3-shaped T=16 and T=8192 layers): 96 beats 0 and
+// 192; clusters of 2 beat 1 and 4.
+#ifndef KT_GEMM_SMALL_N
+#define KT_GEMM_SMALL_N 96
+#endif
+#ifndef KT_GEMM_MAX_CLUSTER
+#define KT_GEMM_MAX_CLUSTER 2
+#endif
+constexpr int kSmallN = KT_GEMM_SMALL_N;      // tiles of at most this many token rows use two-quad stages
+constexpr int kGemmMaxCluster = KT_GEMM_MAX_CLUSTER;
+constexpr int kRing = 176 * 1024;             // stage ring: weight tile + token tile per stage
+constexpr int kMaxCluster = 4;
+static_assert(kGemmMaxCluster == 1 || kGemmMaxCluster == 2 || kGemmMaxCluster == 4, "cluster size");
+constexpr int kSlots = 4;                     // stages in flight at most (barrier pairs, tensor-memory scale slots)
+constexpr int kGroup = 4;                     // K quads per scale group
+constexpr int kSfQuad = 512 + 1024;           // per quad: weight scale block + up to 2 token blocks
+constexpr int kSfBytes = kGroup * kSfQuad;    // one scale-block buffer (two of them)
 constexpr int kStgSFA = 128 * 16;             // staging: 128 weight rows x 16 scale bytes
-constexpr int kStgSFB = kGroup * 256 * 4;     // staging: 4 K steps x 256 token rows x u32
-constexpr int kStgBytes = kStgSFA + kStgSFB;  // one staging buffer (two of them)
+constexpr int kStgSFB = kGroup * 256 * 4;     // staging: 4 quads x 256 token rows x u32
+constexpr int kStgBytes = kStgSFA + kStgSFB;  // one staging buffer
+constexpr int kStgBufs = 3;                   // staging ring: loads run kStgBufs - 1 groups ahead
 constexpr int kEpiBytes = 10240;              // FC1 exchange + transposes / FC2 transpose
-constexpr int kBarBytes = 256;
-constexpr int kSmemTotal = 1024 + kStages * kStageBytes + 2 * kSfBytes + 2 * kStgBytes + kEpiBytes + kBarBytes;
-constexpr int kThreads = 224;
+constexpr int kBarBytes = 512;
+constexpr int kSmemTotal = 1024 + kRing + 2 * kSfBytes + kStgBufs * kStgBytes + kEpiBytes + kBarBytes;
+constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kTileTokens;    // accumulator buffer b at column b * kAccCols
-constexpr uint32_t kTmemSF = 2 * kAccCols;    // scale columns: 12 per stage after both accumulators
-constexpr int kPrefetchGroups = 2;            // scale-warp L2 prefetch distance, in groups of K steps
-static_assert(kStageBytes % 1024 == 0, "stage alignment");
+constexpr uint32_t kTmemSF = 2 * kAccCols;    // scale columns after both accumulators
+constexpr uint32_t kSfSlotCols = 24;          // per stage: 2 quads x (4 weight + 8 token columns)
+constexpr int kPrefetchGroups = 2;            // scale-warp L2 prefetch distance, in groups
+// the largest stage always fits once every earlier stage is released
+static_assert(2 * kQuadW + kSmallN * 256 <= kRing && kQuadW + kTileTokens * 128 <= kRing, "stage ring");
 static_assert(kSmemTotal <= 232448, "shared memory budget");
-static_assert(kTmemSF + 12 * kStages <= kTmemCols, "tensor memory budget");
-static_assert(kTileTokens % 32 == 0 && kTileTokens + 3 <= 256 && kTileTokens <= 240, "token tile");
+static_assert(kTmemSF + kSfSlotCols * kSlots <= kTmemCols, "tensor memory budget");
+static_assert(kTileTokens % (8 * kMaxCluster) == 0 && kTileTokens <= 256 && kChunkRows + 7 <= kTileTokens,
+              "token tile");
+
+constexpr int kMaxShare = kTileTokens / 8;   // 8-row groups one CTA loads per stage, at most
 
 struct TileInfo {
-    int e, f, r0, nvalid, nmma;
+    int e, f;
+    int r_al;     // first token row of the tile (a multiple of 8)
+    int lead;     // rows of another expert before the tile's own: columns [lead, lead + nvalid) are valid
+    int nvalid;
+    int nmma;     // MMA N: lead + nvalid rounded up to a multiple of 16 and of 8 * cluster size
+    int kqs;      // K quads (128 K) per pipeline stage: 2 for small N, 1 otherwise
+};
+
+// Tensor maps of one launch (all in kernel parameter space).
+struct GemmMaps {
+    CUtensorMap w[2];      // weight tile, 1 or 2 K quads per box
+    CUtensorMap t[2][kMaxShare];   // token rows: [quads per stage - 1][8-row groups per box - 1]
+    CUtensorMap wpf;       // packed weight bytes for the L2 prefetch
+    CUtensorMap wsf;       // weight scales, 16-byte rows
+    CUtensorMap asf;       // token scales, K-step-major u32
 };
 
 struct KParams {
     const int32_t* expert_offsets;
     const int32_t* chunk_prefix;
     int E, K, rows_w, I, S, S4, n_ftiles, H;
+    int cl;                   // CTAs per cluster (1, 2 or 4); n_ftiles % cl == 0
+    int nfg;                  // feature-tile groups per chunk: n_ftiles / cl
     const uint8_t* w_sf;      // plain [E * rows_w, K/32] (read directly when K % 512 != 0)
     int sfa_tma;              // 1: weight scales staged by TMA; 0: 4-byte cp.async gathers
     uint8_t* a2;
@@ -93,12 +152,13 @@ struct KParams {
     int debug_flags;
 };
 
-// Tile u -> (expert, feature tile, token chunk); token chunks of one
-// (expert, feature tile) are adjacent so concurrent CTAs share weight tiles
-// through L2.  chunk c of an expert with `cnt` rows split into nc chunks covers
-// rows [c*cnt/nc, (c+1)*cnt/nc).
-__device__ __forceinline__ void decode_tile(const KParams& p, int u, TileInfo& ti) {
-    const int v = u / p.n_ftiles;
+// Work unit u of a cluster -> (expert, feature-tile group, token chunk); the
+// CTA of cluster rank r takes feature tile group * cl + r.  Token chunks of
+// one (expert, feature-tile group) are adjacent so concurrent clusters share
+// weight tiles through L2.  chunk c of an expert with `cnt` rows split into
+// nc chunks covers rows [c*cnt/nc, (c+1)*cnt/nc).
+__device__ __forceinline__ void decode_tile(const KParams& p, int u, int rank, TileInfo& ti) {
+    const int v = u / p.nfg;
     int lo = 1, hi = p.E;                   // first e' with chunk_prefix[e'] > v
     while (lo < hi) {
         const int mid = (lo + hi) >> 1;
@@ -108,22 +168,31 @@ __device__ __forceinline__ void decode_tile(const KParams& p, int u, TileInfo& t
     const int e = lo - 1;
     const int c0 = __ldg(p.chunk_prefix + e);
     const int nc = __ldg(p.chunk_prefix + e + 1) - c0;
-    const int local = u - p.n_ftiles * c0;
+    const int local = u - p.nfg * c0;
     ti.e = e;
-    ti.f = local / nc;
-    const int c = local - ti.f * nc;
+    const int fg = local / nc;
+    ti.f = fg * p.cl + rank;
+    const int c = local - fg * nc;
     const int off = __ldg(p.expert_offsets + e);
     const int cnt = __ldg(p.expert_offsets + e + 1) - off;
     const int a = static_cast<int>(static_cast<long long>(c) * cnt / nc);
     const int b = static_cast<int>(static_cast<long long>(c + 1) * cnt / nc);
-    ti.r0 = off + a;
+    const int r0 = off + a;
+    ti.r_al = r0 & ~7;
+    ti.lead = r0 - ti.r_al;
     ti.nvalid = b - a;
-    ti.nmma = (ti.nvalid + 15) & ~15;
+    const int gran = p.cl > 2 ? 8 * p.cl : 16;
+    ti.nmma = (ti.lead + ti.nvalid + gran - 1) / gran * gran;
+    ti.kqs = ti.nmma <= kSmallN ? 2 : 1;
 }
 
-// Coordinates of a tile's weight rows: for FC1 (3-D view [2E][I][K] of w13)
+__device__ __forceinline__ uint32_t stage_bytes(const TileInfo& ti) {
+    return static_cast<uint32_t>(ti.kqs * (kQuadW + ti.nmma * 128));
+}
+
+// Coordinates of a tile's weight rows: for FC1 (view [2E][I][K] of w13)
 // (y, z) = (64 f, 2 e) selects the 64 gate rows and the 64 matching up rows;
-// otherwise (2-D view [E * rows_w][K]) y = e * rows_w + 128 f.
+// otherwise (view [E * rows_w][K]) y = e * rows_w + 128 f.
 template <int MODE>
 __device__ __forceinline__ void weight_coords(const KParams& p, const TileInfo& ti, int& y, int& z) {
     if (MODE == static_cast<int>(GemmEpilogue::SwiGLU)) {
@@ -139,12 +208,71 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// One lane of a fully active warp (the same lane every call).
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
         "[%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 int z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 int z, int w, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy)
+        : "memory");
+}
+
+// The same box delivered to the same shared-memory offset (and barrier
+// offset) in every CTA of `mask` within the cluster.
+__device__ __forceinline__ void tma_load_4d_mc_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                    int z, int w, uint16_t mask, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7, %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "h"(mask), "l"(policy)
+        : "memory");
+}
+
+// Arrive once on the barrier at offset `bar` of every CTA in `mask` when all
+// tcgen05 operations this thread issued so far have completed.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
 }
 
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
@@ -159,7 +287,7 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x
                  : "memory");
 }
 
-// Load (or prefetch) a weight-side box: 3-D for FC1, 2-D otherwise.
+// Load (or prefetch) a box of the weight-scale / weight-prefetch maps: 3-D for FC1, 2-D otherwise.
 template <int MODE>
 __device__ __forceinline__ void load_weight_box(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
                                                 int z) {
@@ -172,29 +300,113 @@ __device__ __forceinline__ void prefetch_weight_box(const CUtensorMap* map, int 
     else tma_prefetch_l2_2d(map, x, y);
 }
 
-// Walks the (tile, group of kGroup K steps) sequence of one CTA.
+// K-major, 128-byte-swizzled operand descriptor with `sbo` bytes between
+// 8-row groups (1024 when rows are packed, kqs * 1024 for the token layout).
+__device__ __forceinline__ uint64_t sdesc_sw128_sbo(uint32_t saddr, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);          // bits 0-13  start address >> 4
+    d |= static_cast<uint64_t>(16u >> 4) << 16;                    // bits 16-29 leading byte offset (unused)
+    d |= static_cast<uint64_t>(sbo >> 4) << 32;                    // bits 32-45 stride byte offset
+    d |= static_cast<uint64_t>(1u) << 46;                          // bits 46-48 fixed 0b001
+    d |= static_cast<uint64_t>(2u) << 61;                          // bits 61-63 swizzle: 128B
+    return d;
+}
+
+// Placement of stages in the ring: a stage of `need` bytes starts at the
+// head, or at the ring start if it would cross the end.  Offsets are virtual
+// (monotonic); the ring offset is start % kRing.
+struct StageRing {
+    uint64_t head = 0;
+    __device__ __forceinline__ uint64_t place(uint32_t need) {
+        const uint64_t phys = head % kRing;
+        if (phys + need > kRing) head += kRing - phys;
+        const uint64_t start = head;
+        head += need;
+        return start;
+    }
+};
+
+// The consumer's view of the same placement: only the ring offset.
+struct PhysRing {
+    uint32_t phys = 0;
+    __device__ __forceinline__ uint32_t place(uint32_t need) {
+        if (phys + need > static_cast<uint32_t>(kRing)) phys = 0;
+        const uint32_t start = phys;
+        phys += need;
+        return start;
+    }
+};
+
+// Producer-side bookkeeping of the ring: stage gi's bytes end at
+// end_of(gi % kSlots); bytes before `tail` are free; stages below `released`
+// have completed.  Both producer threads run the same stage sequence and so
+// agree on every placement.  acquire() returns the stage's virtual start
+// once its barrier slot and its ring bytes are free, or ~0 on timeout.
+struct RingProducer {
+    StageRing ring;
+    uint64_t b_end0 = 0, b_end1 = 0, b_end2 = 0, b_end3 = 0;   // registers, not a local array
+    uint64_t tail = 0;
+    long long released = 0;
+    static_assert(kSlots == 4, "one end offset per slot");
+    __device__ __forceinline__ uint64_t end_of(int s) const {
+        return s == 0 ? b_end0 : s == 1 ? b_end1 : s == 2 ? b_end2 : b_end3;
+    }
+    __device__ __forceinline__ void set_end(int s, uint64_t v) {
+        if (s == 0) b_end0 = v;
+        else if (s == 1) b_end1 = v;
+        else if (s == 2) b_end2 = v;
+        else b_end3 = v;
+    }
+    __device__ __forceinline__ uint64_t acquire(long long gi, uint32_t need, uint32_t empty_base,
+                                                const volatile int* abort_flag, uint64_t limit) {
+        const int slot = static_cast<int>(gi % kSlots);
+        const uint32_t par = static_cast<uint32_t>((gi / kSlots) & 1) ^ 1u;
+        if (!mbar_wait(empty_base + 8u * slot, par, abort_flag, limit)) return ~0ull;
+        if (gi >= kSlots) {   // stage gi - kSlots (and every earlier one) is done
+            tail = end_of(slot);
+            if (released < gi - kSlots + 1) released = gi - kSlots + 1;
+        }
+        const uint64_t start = ring.place(need);
+        while (start + need - tail > static_cast<uint64_t>(kRing)) {
+            // wait for the oldest stage still holding ring bytes
+            const long long j = released;
+            const int js = static_cast<int>(j % kSlots);
+            if (!mbar_wait(empty_base + 8u * js, static_cast<uint32_t>((j / kSlots) & 1), abort_flag, limit))
+                return ~0ull;
+            tail = end_of(js);
+            released = j + 1;
+        }
+        set_end(slot, start + need);
+        return start;
+    }
+};
+
+// Walks the (work unit, group of kGroup K quads) sequence of one CTA.
 template <int MODE>
 struct GroupCursor {
-    int u, g;          // tile id and group index within the tile
+    int u, g;          // work unit and group index within the tile
     TileInfo ti;
     int wy, wz;
     bool valid;
-    __device__ __forceinline__ void start(const KParams& p, int total) {
-        u = blockIdx.x;
+    int rank, stride;
+    __device__ __forceinline__ void start(const KParams& p, int total, int first, int rank_, int stride_) {
+        u = first;
+        rank = rank_;
+        stride = stride_;
         g = 0;
         load(p, total);
     }
     __device__ __forceinline__ void load(const KParams& p, int total) {
         valid = u < total;
         if (valid) {
-            decode_tile(p, u, ti);
+            decode_tile(p, u, rank, ti);
             weight_coords<MODE>(p, ti, wy, wz);
         }
     }
     __device__ __forceinline__ void advance(const KParams& p, int total, int ngroups) {
         if (++g == ngroups) {
             g = 0;
-            u += gridDim.x;
+            u += stride;
             load(p, total);
         }
     }
@@ -202,47 +414,51 @@ struct GroupCursor {
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    mx_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b16,
-                   const __grid_constant__ CUtensorMap map_b32, const __grid_constant__ CUtensorMap map_b64,
-                   const __grid_constant__ CUtensorMap map_b128, const __grid_constant__ CUtensorMap map_wpf,
-                   const __grid_constant__ CUtensorMap map_wsf, const __grid_constant__ CUtensorMap map_asf,
-                   const __grid_constant__ KParams p) {
+    mx_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ KParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    const uint32_t s_base = smem_u32(smem);
-    uint8_t* sfbuf = smem + kStages * kStageBytes;        // two scale-block buffers
-    uint8_t* stg = sfbuf + 2 * kSfBytes;                   // two staging buffers
-    uint8_t* epi = stg + 2 * kStgBytes;
+    const uint32_t ring_base = smem_u32(smem);             // stage ring
+    uint8_t* sfbuf = smem + kRing;                         // two scale-block buffers
+    uint8_t* stg = sfbuf + 2 * kSfBytes;                   // staging ring
+    uint8_t* epi = stg + kStgBufs * kStgBytes;
     uint8_t* bars = epi + kEpiBytes;
     const uint32_t bar_base = smem_u32(bars);
-    // barriers: full[4] empty[4] sf_full[2] sf_empty[2] stg[2] acc_full[2] acc_empty[2] drain
-    auto full_bar = [&](int s) { return bar_base + 8u * s; };
-    auto empty_bar = [&](int s) { return bar_base + 8u * (4 + s); };
-    auto sf_full = [&](int b) { return bar_base + 8u * (8 + b); };
-    auto sf_empty = [&](int b) { return bar_base + 8u * (10 + b); };
-    auto stg_bar = [&](int b) { return bar_base + 8u * (12 + b); };
-    auto acc_full = [&](int b) { return bar_base + 8u * (14 + b); };
-    auto acc_empty = [&](int b) { return bar_base + 8u * (16 + b); };
-    const uint32_t drain_bar = bar_base + 8u * 18;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 192);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 200);
+    // barriers: full[S] empty[S] sf_full[2] sf_empty[2] stg[3] acc_full[2] acc_empty[2] drain
+    const uint32_t full_base = bar_base;
+    const uint32_t empty_base = bar_base + 8u * kSlots;
+    auto full_bar = [&](int s) { return full_base + 8u * s; };
+    auto empty_bar = [&](int s) { return empty_base + 8u * s; };
+    auto sf_full = [&](int b) { return bar_base + 8u * (2 * kSlots + b); };
+    auto sf_empty = [&](int b) { return bar_base + 8u * (2 * kSlots + 2 + b); };
+    auto stg_bar = [&](int b) { return bar_base + 8u * (2 * kSlots + 4 + b); };
+    auto acc_full = [&](int b) { return bar_base + 8u * (2 * kSlots + 4 + kStgBufs + b); };
+    auto acc_empty = [&](int b) { return bar_base + 8u * (2 * kSlots + 6 + kStgBufs + b); };
+    const uint32_t drain_bar = bar_base + 8u * (2 * kSlots + 8 + kStgBufs);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 480);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 488);
+    static_assert(8 * (2 * kSlots + 9 + kStgBufs) <= 480, "barrier area");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int cl = p.cl;
+    const int rank = cl > 1 ? static_cast<int>(cluster_rank()) : 0;
+    const int first = static_cast<int>(blockIdx.x) / cl;      // this cluster's first work unit
+    const int stride = static_cast<int>(gridDim.x) / cl;      // clusters in the grid
+    const uint16_t cl_mask = static_cast<uint16_t>((1u << cl) - 1u);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_bar(s), 1);      // producer's arrive.expect_tx
-            mbar_init(empty_bar(s), 1);     // tcgen05.commit
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(full_bar(s), 2);      // one arrive.expect_tx per producer thread
+            mbar_init(empty_bar(s), cl);    // one tcgen05.commit per CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(sf_full(b), 32);      // one arrive per scale-warp lane
             mbar_init(sf_empty(b), 1);      // tcgen05.commit
-            mbar_init(stg_bar(b), 1);       // scale warp's arrive.expect_tx
             mbar_init(acc_full(b), 1);      // tcgen05.commit
             mbar_init(acc_empty(b), 4);     // one arrive per epilogue warp
         }
+        for (int b = 0; b < kStgBufs; ++b) mbar_init(stg_bar(b), 1);   // scale warp's arrive.expect_tx
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -253,74 +469,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_relinquish();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&map_w);
-        tma_prefetch_map(&map_b16);
-        tma_prefetch_map(&map_b32);
-        tma_prefetch_map(&map_b64);
-        tma_prefetch_map(&map_b128);
+        tma_prefetch_map(&maps.w[0]);
+        tma_prefetch_map(&maps.w[1]);
+    }
+    if (warp == 3) {
+        for (int i = lane; i < 2 * kMaxShare; i += 32) tma_prefetch_map(&maps.t[i / kMaxShare][i % kMaxShare]);
     }
     if (warp == 2 && lane == 0) {
-        tma_prefetch_map(&map_wpf);
-        tma_prefetch_map(&map_asf);
-        if (p.sfa_tma) tma_prefetch_map(&map_wsf);
+        tma_prefetch_map(&maps.wpf);
+        tma_prefetch_map(&maps.asf);
+        if (p.sfa_tma) tma_prefetch_map(&maps.wsf);
     }
     tc_fence_before();
     __syncthreads();
+    if (cl > 1) cluster_sync_all();   // every CTA's barriers exist before any multicast lands
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int total = p.n_ftiles * __ldg(p.chunk_prefix + p.E);
-    const int nk = p.K / kBK;
-    const int ngroups = (nk + kGroup - 1) / kGroup;
+    const int total = p.nfg * __ldg(p.chunk_prefix + p.E);   // work units of the grid's clusters
+    const int nq = p.K / 128;                  // K quads per tile
+    const int ngroups = (nq + kGroup - 1) / kGroup;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp == 0 || warp == 3) {
+        // ------------------------------------------------------------ producers (one lane each)
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
+            const bool weights = warp == 0;
             bool ok = true;
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_a = l2_policy_evict_last();
-            const CUtensorMap* bmaps[4] = {&map_b16, &map_b32, &map_b64, &map_b128};
-            for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+            RingProducer rp;
+            long long gi = 0;
+            for (int u = first; u < total && ok; u += stride) {
                 TileInfo ti;
-                decode_tile(p, u, ti);
+                decode_tile(p, u, rank, ti);
                 int wy, wz;
                 weight_coords<MODE>(p, ti, wy, wz);
-                const uint32_t tx = static_cast<uint32_t>(kTxA + ti.nmma * kBK);
-                for (int kb = 0; kb < nk; ++kb) {
-                    ok = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns);
-                    if (!ok) break;
-                    const bool withhold = (p.debug_flags & KT_DEBUG_WITHHOLD_STAGE) &&
-                                          u == static_cast<int>(blockIdx.x) && kb == 0;
-                    if (!withhold) {   // test hook: a withheld stage is neither loaded nor signalled
-                        const uint32_t sA = s_base + stage * kStageBytes;
-                        const uint32_t sB = sA + kSmemA;
-                        mbar_arrive_expect_tx(full_bar(stage), tx);
-                        if (MODE == static_cast<int>(GemmEpilogue::SwiGLU)) {
-                            asm volatile(
-                                "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                                ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(sA),
-                                "l"(reinterpret_cast<uint64_t>(&map_w)), "r"(full_bar(stage)), "r"(kb * kBK),
-                                "r"(wy), "r"(wz), "l"(pol_w)
-                                : "memory");
-                        } else {
-                            tma_load_2d_hint(sA, &map_w, full_bar(stage), kb * kBK, wy, pol_w);
-                        }
-                        int rdone = 0;
-#pragma unroll
-                        for (int bi = 3; bi >= 0; --bi) {
-                            const int rows = 16 << bi;
-                            if (ti.nmma - rdone >= rows) {
-                                tma_load_2d_hint(sB + rdone * kBK, bmaps[bi], full_bar(stage), kb * kBK,
-                                                 ti.r0 + rdone, pol_a);
-                                rdone += rows;
-                            }
-                        }
+                const uint32_t need = stage_bytes(ti);
+                const int nk = (nq + ti.kqs - 1) / ti.kqs;
+                const int share = (ti.nmma >> 3) / cl;            // 8-row groups this CTA loads
+                const int g0 = (ti.r_al >> 3) + rank * share;
+                const uint32_t gstride = static_cast<uint32_t>(ti.kqs) * 1024u;   // bytes per 8-row group
+                const CUtensorMap* tm = &maps.t[ti.kqs - 1][share - 1];   // one box covers this CTA's share
+                for (int kb = 0; kb < nk; ++kb, ++gi) {
+                    const uint64_t start = rp.acquire(gi, need, empty_base, abort_flag, p.wait_limit_ns);
+                    if (start == ~0ull) {
+                        ok = false;
+                        break;
                     }
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
+                    const int slot = static_cast<int>(gi % kSlots);
+                    const bool withhold = (p.debug_flags & KT_DEBUG_WITHHOLD_STAGE) && u == first && kb == 0;
+                    if (withhold) continue;   // test hook: a withheld stage is neither loaded nor signalled
+                    const uint32_t dst = ring_base + static_cast<uint32_t>(start % kRing);
+                    const int kq0 = kb * ti.kqs;
+                    if (weights) {
+                        mbar_arrive_expect_tx(full_bar(slot), kQuadWTx * ti.kqs);
+                        const CUtensorMap* wm = &maps.w[ti.kqs - 1];
+                        if (MODE == static_cast<int>(GemmEpilogue::SwiGLU))
+                            tma_load_4d_hint(dst, wm, full_bar(slot), 0, wy, wz, kq0, pol_w);
+                        else
+                            tma_load_3d_hint(dst, wm, full_bar(slot), 0, wy, kq0, pol_w);
+                    } else {
+                        // this CTA's expected bytes: the whole token tile, from every CTA's share
+                        mbar_arrive_expect_tx(full_bar(slot), static_cast<uint32_t>(ti.nmma * 128 * ti.kqs));
+                        const uint32_t tdst = dst + static_cast<uint32_t>(ti.kqs * kQuadW) +
+                                              static_cast<uint32_t>(rank * share) * gstride;
+                        if (cl > 1)
+                            tma_load_4d_mc_hint(tdst, tm, full_bar(slot), 0, 0, kq0, g0, cl_mask, pol_a);
+                        else
+                            tma_load_4d_hint(tdst, tm, full_bar(slot), 0, 0, kq0, g0, pol_a);
                     }
                 }
             }
@@ -331,52 +547,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------ scale warp
-        uint32_t stg_ph[2] = {0u, 0u}, sfe_ph[2] = {0u, 0u};
+        uint32_t stg_ph = 0u, sfe_ph = 0u;   // one parity bit per buffer
         bool ok = true;
         const uint32_t stg_tx = static_cast<uint32_t>(kStgSFB + (p.sfa_tma ? kStgSFA : 0));
         const int ksf = p.K / 32;
-        GroupCursor<MODE> cur, nxt, pf;
-        cur.start(p, total);
-        nxt = cur;
+        GroupCursor<MODE> cur, ahead, pf;
+        cur.start(p, total, first, rank, stride);
+        ahead = cur;
         pf = cur;
         auto issue_staging = [&](const GroupCursor<MODE>& c, int buf) {
             if (lane == 0 && c.valid) {
                 const uint32_t dst = smem_u32(stg + buf * kStgBytes);
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(stg_bar(buf), stg_tx);
-                if (p.sfa_tma) load_weight_box<MODE>(dst, &map_wsf, stg_bar(buf), c.g * 16, c.wy, c.wz);
-                tma_load_2d(dst + kStgSFA, &map_asf, stg_bar(buf), c.ti.r0 & ~3, c.g * kGroup);
+                if (p.sfa_tma) load_weight_box<MODE>(dst, &maps.wsf, stg_bar(buf), c.g * 16, c.wy, c.wz);
+                tma_load_2d(dst + kStgSFA, &maps.asf, stg_bar(buf), c.ti.r_al, c.g * kGroup);
             }
         };
         auto prefetch_group = [&](const GroupCursor<MODE>& c) {
-            if (lane == 0 && c.valid) prefetch_weight_box<MODE>(&map_wpf, c.g * (kGroup * kBK / 2), c.wy, c.wz);
+            if (lane == 0 && c.valid) prefetch_weight_box<MODE>(&maps.wpf, c.g * (kGroup * 128 / 2), c.wy, c.wz);
         };
         for (int i = 0; i < kPrefetchGroups; ++i) {
             prefetch_group(pf);
             pf.advance(p, total, ngroups);
         }
-        issue_staging(cur, 0);
-        int buf = 0;
+        for (int i = 0; i < kStgBufs - 1; ++i) {   // staging for the first groups
+            issue_staging(ahead, i);
+            ahead.advance(p, total, ngroups);
+        }
+        int gidx = 0;
         while (cur.valid && ok) {
-            nxt = cur;
-            nxt.advance(p, total, ngroups);
-            __syncwarp();                      // every lane is done with the buffer refilled next
-            issue_staging(nxt, buf ^ 1);
+            const int sbuf = gidx % kStgBufs;     // staging buffer of this group
+            const int fbuf = gidx & 1;            // scale-block buffer of this group
+            __syncwarp();                         // every lane is done with the buffer refilled next
+            issue_staging(ahead, (gidx + kStgBufs - 1) % kStgBufs);
+            ahead.advance(p, total, ngroups);
             prefetch_group(pf);
             pf.advance(p, total, ngroups);
-            ok = __all_sync(0xffffffffu, mbar_wait(stg_bar(buf), stg_ph[buf], abort_flag, p.wait_limit_ns));
+            ok = __all_sync(0xffffffffu, mbar_wait(stg_bar(sbuf), (stg_ph >> sbuf) & 1u, abort_flag,
+                                                   p.wait_limit_ns));
             if (!ok) break;
-            ok = __all_sync(0xffffffffu, mbar_wait(sf_empty(buf), sfe_ph[buf] ^ 1u, abort_flag, p.wait_limit_ns));
+            ok = __all_sync(0xffffffffu, mbar_wait(sf_empty(fbuf), ((sfe_ph >> fbuf) & 1u) ^ 1u, abort_flag,
+                                                   p.wait_limit_ns));
             if (!ok) break;
             const TileInfo& ti = cur.ti;
-            const uint8_t* sb = stg + buf * kStgBytes;
-            uint8_t* sfo = sfbuf + buf * kSfBytes;
-            const int kb0 = cur.g * kGroup;
-            const int nkk = min(kGroup, nk - kb0);
-            const int shift = ti.r0 & 3;
+            const uint8_t* sb = stg + sbuf * kStgBytes;
+            uint8_t* sfo = sfbuf + fbuf * kSfBytes;
+            const int kq0 = cur.g * kGroup;
+            const int nkk = min(kGroup, nq - kq0);
             const int natoms = ti.nmma > 128 ? 2 : 1;
+            const int lo = ti.lead, hi = ti.lead + ti.nvalid;
             for (int kk = 0; kk < nkk; ++kk) {
-                uint8_t* blk = sfo + kk * kSfStep;
+                uint8_t* blk = sfo + kk * kSfQuad;
                 // weight scales: tile row r -> byte (r%32)*16 + (r/32)*4 of the 512-byte block
                 if (p.sfa_tma) {
                     uint32_t w4[4];
@@ -393,29 +615,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                             grow = static_cast<size_t>(ti.e) * p.rows_w + (r < 64 ? 0 : p.I) + ti.f * 64 + (r & 63);
                         else
                             grow = static_cast<size_t>(ti.e) * p.rows_w + ti.f * 128 + r;
-                        cp_async_4(smem_u32(blk + lane * 16 + i * 4), p.w_sf + grow * ksf + (kb0 + kk) * 4, 4);
+                        cp_async_4(smem_u32(blk + lane * 16 + i * 4), p.w_sf + grow * ksf + (kq0 + kk) * 4, 4);
                     }
                 }
-                // token scales from the K-step-major staging rows (shifted by r0 % 4)
-                const uint32_t* arow = reinterpret_cast<const uint32_t*>(sb + kStgSFA) + kk * 256 + shift;
+                // token scales from the K-step-major staging rows (tile column t = row r_al + t)
+                const uint32_t* arow = reinterpret_cast<const uint32_t*>(sb + kStgSFA) + kk * 256;
                 for (int a = 0; a < natoms; ++a) {
                     uint32_t t4[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int t = 128 * a + lane + 32 * i;
-                        t4[i] = (t < ti.nvalid) ? arow[t] : 0u;
+                        t4[i] = (t >= lo && t < hi) ? arow[t] : 0u;
                     }
                     *reinterpret_cast<uint4*>(blk + 512 + a * 512 + lane * 16) =
                         make_uint4(t4[0], t4[1], t4[2], t4[3]);
                 }
             }
             fence_proxy_async_smem();
-            if (p.sfa_tma) mbar_arrive(sf_full(buf));
-            else cp_async_arrive_noinc(sf_full(buf));
-            stg_ph[buf] ^= 1u;
-            sfe_ph[buf] ^= 1u;
-            buf ^= 1;
-            cur = nxt;
+            if (p.sfa_tma) mbar_arrive(sf_full(fbuf));
+            else cp_async_arrive_noinc(sf_full(fbuf));
+            stg_ph ^= 1u << sbuf;
+            sfe_ph ^= 1u << fbuf;
+            ++gidx;
+            cur.advance(p, total, ngroups);
         }
         if (!ok) {
             if (lane == 0) set_error(p.err, KT_DEVERR_TIMEOUT_LOAD);
@@ -423,86 +645,113 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            int stage = 0, sb = 0, it = 0;
-            uint32_t phase = 0;
-            uint32_t acc_ph[2] = {0u, 0u}, sf_ph[2] = {0u, 0u};
+        // The whole warp follows the pipeline (measured faster on GB300 than one
+        // lane running it alone); one elected lane issues the tensor-core work.
+        {
+            auto wait = [&](uint32_t bar, uint32_t par) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag, p.wait_limit_ns));
+            };
+            auto leader = [&]() -> bool { return elect_one_sync(); };
+            auto wsync = [&]() { __syncwarp(); };
+            int sb = 0, it = 0;
+            long long gi = 0;
+            PhysRing ring;
+            uint32_t acc_ph = 0u, sf_ph = 0u;   // one parity bit per buffer
             bool ok = true, issued = false;
-            for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++it) {
+            for (int u = first; u < total && ok; u += stride, ++it) {
                 TileInfo ti;
-                decode_tile(p, u, ti);
+                decode_tile(p, u, rank, ti);
                 const int ab = it & 1;
                 issued = true;
-                ok = mbar_wait(acc_empty(ab), acc_ph[ab] ^ 1u, abort_flag, p.wait_limit_ns);
+                ok = wait(acc_empty(ab), ((acc_ph >> ab) & 1u) ^ 1u);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + ab * kAccCols;
                 const uint32_t idesc0 = idesc_mx_e2m1_e4m3(ti.nmma, 0);
-                for (int kb = 0; kb < nk; ++kb) {
-                    const int kk = kb & (kGroup - 1);
-                    if (kk == 0) {
-                        ok = mbar_wait(sf_full(sb), sf_ph[sb], abort_flag, p.wait_limit_ns);
-                        if (!ok) break;
-                        fence_proxy_async_smem();   // scale blocks were written through the generic proxy
-                    }
-                    ok = mbar_wait(full_bar(stage), phase, abort_flag, p.wait_limit_ns);
+                const uint32_t need = stage_bytes(ti);
+                const int nk = (nq + ti.kqs - 1) / ti.kqs;
+                const uint32_t tok_sbo = static_cast<uint32_t>(ti.kqs) * 1024u;
+                for (int kb = 0; kb < nk && ok; ++kb, ++gi) {
+                    const uint32_t off = ring.place(need);
+                    const int slot = static_cast<int>(gi % kSlots);
+                    const int kq0 = kb * ti.kqs;
+                    const int nqs = min(ti.kqs, nq - kq0);     // K quads in this stage
+                    const int kq_last = kq0 + nqs - 1;
+                    // a stage never straddles scale groups: it starts a group when kq0 % kGroup == 0
+                    const bool group_start = (kq0 & (kGroup - 1)) == 0;
+                    const bool group_end = (kq_last & (kGroup - 1)) == kGroup - 1 || kq_last == nq - 1;
+                    ok = wait(full_bar(slot), static_cast<uint32_t>((gi / kSlots) & 1));
                     if (!ok) break;
+                    if (group_start) {
+                        ok = wait(sf_full(sb), (sf_ph >> sb) & 1u);
+                        if (!ok) break;
+                        // blocks gathered by cp.async were written through the generic proxy; the
+                        // TMA-staged path fences on the writer's side before it arrives
+                        if (!p.sfa_tma) fence_proxy_async_smem();
+                    }
                     tc_fence_after();
-                    const uint32_t sA = s_base + stage * kStageBytes;
-                    const uint32_t sB = sA + kSmemA;
-                    const uint32_t sF = smem_u32(sfbuf + sb * kSfBytes + kk * kSfStep);
-                    const uint32_t t_sfa = tmem + kTmemSF + stage * 12;
-                    const uint32_t t_sfb = t_sfa + 4;
-                    tc_cp_32x128b_warpx4(t_sfa, sdesc_sf_block(sF));
-                    tc_cp_32x128b_warpx4(t_sfb, sdesc_sf_block(sF + 512));
-                    if (ti.nmma > 128) tc_cp_32x128b_warpx4(t_sfb + 4, sdesc_sf_block(sF + 1024));
+                    if (leader()) {
+                        for (int q = 0; q < nqs; ++q) {
+                            const int kk = (kq0 + q) & (kGroup - 1);
+                            const uint32_t sA = ring_base + off + q * kQuadW;
+                            const uint32_t sB = ring_base + off + ti.kqs * kQuadW + q * 1024;
+                            const uint32_t sF = smem_u32(sfbuf + sb * kSfBytes + kk * kSfQuad);
+                            const uint32_t t_sfa = tmem + kTmemSF + slot * kSfSlotCols + q * 12;
+                            const uint32_t t_sfb = t_sfa + 4;
+                            tc_cp_32x128b_warpx4(t_sfa, sdesc_sf_block(sF));
+                            tc_cp_32x128b_warpx4(t_sfb, sdesc_sf_block(sF + 512));
+                            if (ti.nmma > 128) tc_cp_32x128b_warpx4(t_sfb + 4, sdesc_sf_block(sF + 1024));
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t idesc =
-                            idesc0 | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
-                        tc_mma_mxf8f6f4(d_tmem, sdesc_k_sw128(sA + 32 * j), sdesc_k_sw128(sB + 32 * j), idesc, t_sfa,
-                                        t_sfb, (kb | j) != 0 ? 1u : 0u);
+                            for (int j = 0; j < 4; ++j) {
+                                const uint32_t idesc =
+                                    idesc0 | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
+                                tc_mma_mxf8f6f4(d_tmem, sdesc_sw128_sbo(sA + 32 * j, 1024),
+                                                sdesc_sw128_sbo(sB + 32 * j, tok_sbo), idesc, t_sfa, t_sfb,
+                                                ((kq0 + q) | j) != 0 ? 1u : 0u);
+                            }
+                        }
+                        if (group_end) tc_commit(sf_empty(sb));
+                        if (cl > 1) tc_commit_mc(empty_bar(slot), cl_mask);   // frees the stage in every CTA
+                        else tc_commit(empty_bar(slot));
                     }
-                    tc_commit(empty_bar(stage));
-                    if (kk == kGroup - 1 || kb == nk - 1) {
-                        tc_commit(sf_empty(sb));
-                        sf_ph[sb] ^= 1u;
+                    wsync();
+                    if (group_end) {
+                        sf_ph ^= 1u << sb;
                         sb ^= 1;
-                    }
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(acc_full(ab));
-                acc_ph[ab] ^= 1u;
+                if (leader()) tc_commit(acc_full(ab));
+                wsync();
+                acc_ph ^= 1u << ab;
             }
             if (!ok) {
-                set_error(p.err, KT_DEVERR_TIMEOUT_MMA);
+                if (lane == 0) set_error(p.err, KT_DEVERR_TIMEOUT_MMA);
                 *abort_flag = 1;
             }
             // every tcgen05 operation issued above completes before teardown
             if (issued) {
-                tc_commit(drain_bar);
-                mbar_wait(drain_bar, 0, abort_flag, p.wait_limit_ns);
+                if (leader()) tc_commit(drain_bar);
+                wsync();
+                wait(drain_bar, 0);
             }
         }
     } else {
-        // ------------------------------------------------------------ epilogue (warps 3-6)
+        // ------------------------------------------------------------ epilogue (warps 4-7)
         const int q = warp & 3;                        // tensor-memory lane quadrant
-        uint32_t acc_ph[2] = {0u, 0u};
+        uint32_t acc_ph = 0u;                          // one parity bit per buffer
         int it = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++it) {
+        for (int u = first; u < total && ok; u += stride, ++it) {
             TileInfo ti;
-            decode_tile(p, u, ti);
+            decode_tile(p, u, rank, ti);
             const int ab = it & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(acc_full(ab), acc_ph[ab], abort_flag, p.wait_limit_ns));
+            ok = __all_sync(0xffffffffu, mbar_wait(acc_full(ab), (acc_ph >> ab) & 1u, abort_flag, p.wait_limit_ns));
             if (!ok) break;
             tc_fence_after();
             const uint32_t trow = tmem + ab * kAccCols + (static_cast<uint32_t>(32 * q) << 16);
-            for (int c0 = 0; c0 < ti.nvalid; c0 += 32) {
+            const int lo = ti.lead, hi = ti.lead + ti.nvalid;
+            for (int c0 = 0; c0 < hi; c0 += 32) {
                 uint32_t v[32];
                 tc_ld_32x32b_x32(trow + static_cast<uint32_t>(c0), v);
                 tc_wait_ld();
@@ -510,17 +759,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int n = ti.f * 128 + q * 32 + lane;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        if (c0 + j < ti.nvalid)
-                            p.raw_out[static_cast<size_t>(ti.r0 + c0 + j) * p.rows_w + n] = __uint_as_float(v[j]);
+                        if (c0 + j >= lo && c0 + j < hi)
+                            p.raw_out[static_cast<size_t>(ti.r_al + c0 + j) * p.rows_w + n] = __uint_as_float(v[j]);
                     }
                 } else if (MODE == static_cast<int>(GemmEpilogue::Combine)) {
                     // weight, round to bf16 and transpose through shared memory so each
                     // lane writes 64 contiguous bytes of one token's output row
                     uint8_t* tb = epi + q * 2560;   // [32 tokens][80 bytes]
+                    const bool mine = c0 + lane >= lo && c0 + lane < hi;
                     int slot = 0;
                     float wt = 0.f;
-                    if (c0 + lane < ti.nvalid) {
-                        slot = __ldg(p.perm + ti.r0 + c0 + lane);
+                    if (mine) {
+                        slot = __ldg(p.perm + ti.r_al + c0 + lane);
                         wt = __ldg(p.topk_w + slot);
                     }
 #pragma unroll
@@ -530,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<__nv_bfloat16*>(tb + j * 80 + lane * 2) = b;
                     }
                     __syncwarp();
-                    if (c0 + lane < ti.nvalid) {
+                    if (mine) {
                         const uint4* src = reinterpret_cast<const uint4*>(tb + lane * 80);
                         uint4* dst =
                             reinterpret_cast<uint4*>(p.y + static_cast<size_t>(slot) * p.H + ti.f * 128 + q * 32);
@@ -543,12 +793,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     // SwiGLU.  Quadrants 0,1 hold gate rows (features 32q + lane of the
                     // tile), 2,3 the matching up rows.  The pair (q, q+2) splits the 32
-                    // tokens: the gate warp finishes tokens 0-15, the up warp 16-31,
+                    // columns: the gate warp finishes columns 0-15, the up warp 16-31,
                     // each taking the partner's half of the values through shared memory.
                     const int pair = q & 1;
                     const bool gate = q < 2;
-                    float* X = reinterpret_cast<float*>(epi) + pair * 512;          // silu(gate), tokens 16-31
-                    float* Y = reinterpret_cast<float*>(epi) + 1024 + pair * 512;   // up, tokens 0-15
+                    float* X = reinterpret_cast<float*>(epi) + pair * 512;          // silu(gate), columns 16-31
+                    float* Y = reinterpret_cast<float*>(epi) + 1024 + pair * 512;   // up, columns 0-15
                     if (gate) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
@@ -560,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 16; ++j) Y[j * 32 + lane] = __uint_as_float(v[j]);
                     }
                     named_bar_sync(1, 128);
-                    uint8_t* my_bt = epi + 8192 + q * 512;   // [16 tokens][32 features]
+                    uint8_t* my_bt = epi + 8192 + q * 512;   // [16 columns][32 features]
                     uint8_t my_scale = 0;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
@@ -577,9 +827,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (lane == j) my_scale = static_cast<uint8_t>(X8 + 127);
                     }
                     __syncwarp();
-                    const int tok = c0 + (gate ? 0 : 16) + lane;
-                    if (lane < 16 && tok < ti.nvalid) {
-                        const size_t row = static_cast<size_t>(ti.r0 + tok);
+                    const int col_t = c0 + (gate ? 0 : 16) + lane;
+                    if (lane < 16 && col_t >= lo && col_t < hi) {
+                        const size_t row = static_cast<size_t>(ti.r_al + col_t);
                         const int col = ti.f * 64 + pair * 32;
                         const uint4* srcv = reinterpret_cast<const uint4*>(my_bt + lane * 32);
                         uint4* dst = reinterpret_cast<uint4*>(p.a2 + row * p.I + col);
@@ -594,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty(ab));
-            acc_ph[ab] ^= 1u;
+            acc_ph ^= 1u << ab;
         }
         if (!ok) {
             if (lane == 0) set_error(p.err, KT_DEVERR_TIMEOUT_EPI);
@@ -604,7 +854,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag) __nanosleep(1000000);   // let any copy still in flight land before teardown
+    if (*abort_flag) __nanosleep(1000000);   // let any copy or commit still in flight land before teardown
+    // no CTA leaves while a peer may still multicast into it or arrive on its barriers
+    if (cl > 1) cluster_sync_all();
     if (warp == 1) {
         tc_fence_after();
         tc_dealloc(tmem, kTmemCols);
@@ -626,13 +878,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// rank-2 or rank-3 tiled map (dims/box innermost first; strides in bytes for dims 1..rank-1)
+// tiled map of rank 2-4 (dims/box innermost first; strides in bytes for dims 1..rank-1)
 static bool encode(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank, const uint64_t* dims,
                    const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t d[3], st[2];
-    cuuint32_t b[3], es[3] = {1, 1, 1};
+    cuuint64_t d[4], st[3];
+    cuuint32_t b[4], es[4] = {1, 1, 1, 1};
     for (int i = 0; i < rank; ++i) {
         d[i] = dims[i];
         b[i] = box[i];
@@ -643,8 +895,53 @@ static bool encode(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Largest cluster size (up to `want`) whose co-resident clusters of one CTA
+// per SM cover at least 15/16 of the SMs; asked of the driver once per device.
 template <int MODE>
-static cudaError_t launch_mode(const CUtensorMap* maps, const KParams& kp, cudaStream_t s) {
+static int pick_cluster(int want, int* grid) {
+    static int best_c[64][3] = {}, best_g[64][3] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int sms = sm_count();
+    const int idx = want >= 4 ? 2 : want >= 2 ? 1 : 0;
+    if (dev < 64 && best_c[dev][idx] != 0) {
+        *grid = best_g[dev][idx];
+        return best_c[dev][idx];
+    }
+    int c_pick = 1, g_pick = sms;
+    for (int c = want; c >= 2; c /= 2) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(sms / c * c));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemTotal;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int nclusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&nclusters, mx_gemm_kernel<MODE>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (nclusters * c * 16 >= sms * 15) {
+            c_pick = c;
+            g_pick = nclusters * c;
+            break;
+        }
+    }
+    if (dev < 64) {
+        best_c[dev][idx] = c_pick;
+        best_g[dev][idx] = g_pick;
+    }
+    *grid = g_pick;
+    return c_pick;
+}
+
+template <int MODE>
+static cudaError_t launch_mode(const GemmMaps& maps, KParams kp, int max_cluster, cudaStream_t s) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -654,71 +951,97 @@ static cudaError_t launch_mode(const CUtensorMap* maps, const KParams& kp, cudaS
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    mx_gemm_kernel<MODE><<<sm_count(), kThreads, kSmemTotal, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
-                                                                   maps[5], maps[6], maps[7], kp);
+    int want = 1;
+    if (kp.n_ftiles % 4 == 0 && max_cluster >= 4) want = 4;
+    else if (kp.n_ftiles % 2 == 0 && max_cluster >= 2) want = 2;
+    int grid = sm_count();
+    const int c = want > 1 ? pick_cluster<MODE>(want, &grid) : 1;
+    kp.cl = c;
+    kp.nfg = kp.n_ftiles / c;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemTotal;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = c > 1 ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, mx_gemm_kernel<MODE>, maps, kp);
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 kt_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
     if (a.S <= 0) return KT_OK;
-    // 0 weight tile (fp4 unpacked), 1-4 token boxes of 16/32/64/128 rows,
-    // 5 weight bytes for the L2 prefetch, 6 weight scales (16-byte rows),
-    // 7 token scales (K-step-major u32)
-    alignas(64) CUtensorMap maps[8];
+    alignas(64) GemmMaps maps;
     const bool fc1 = a.mode == GemmEpilogue::SwiGLU;
     const uint64_t K = static_cast<uint64_t>(a.K);
     const uint64_t wrows = static_cast<uint64_t>(a.E) * a.rows_w;
     const int S4 = sf_rows(a.S);
     const bool sfa_tma = (a.K % 512) == 0;
     bool ok = true;
+    for (int kq = 1; kq <= 2; ++kq) {
+        if (fc1) {
+            // w13 viewed as [K/128 quad][2E][I][128]: (z = 2e + gate/up, y = row within the half)
+            const uint64_t dw[4] = {128, static_cast<uint64_t>(a.I), 2ull * a.E, K / 128};
+            const uint64_t sw[3] = {K / 2, static_cast<uint64_t>(a.I) * (K / 2), 64};
+            const uint32_t bw[4] = {128, 64, 2, static_cast<uint32_t>(kq)};
+            ok = ok && encode(&maps.w[kq - 1], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.w, 4, dw, sw, bw,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+        } else {
+            // w viewed as [K/128 quad][E * rows_w][128]
+            const uint64_t dw[3] = {128, wrows, K / 128};
+            const uint64_t sw[2] = {K / 2, 64};
+            const uint32_t bw[3] = {128, 128, static_cast<uint32_t>(kq)};
+            ok = ok && encode(&maps.w[kq - 1], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.w, 3, dw, sw, bw,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+        }
+        // activations viewed as [S8/8 group][K/128 quad][8 rows][128]; rows up
+        // to S8 = S rounded up to 8 must be addressable (callers pad the buffer)
+        const uint64_t S8 = (static_cast<uint64_t>(a.S) + 7) / 8 * 8;
+        for (int g = 1; g <= kMaxShare; ++g) {
+            const uint64_t db[4] = {128, 8, K / 128, S8 / 8};
+            const uint64_t sb[3] = {K, 128, 8 * K};
+            const uint32_t bb[4] = {128, 8, static_cast<uint32_t>(kq), static_cast<uint32_t>(g)};
+            ok = ok && encode(&maps.t[kq - 1][g - 1], CU_TENSOR_MAP_DATA_TYPE_UINT8, a.act, 4, db, sb, bb,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+        }
+    }
     if (fc1) {
-        // w13 viewed as [2E][I][K]: (z = 2e + half, y = row within the half)
-        const uint64_t dw[3] = {K, static_cast<uint64_t>(a.I), 2ull * a.E};
-        const uint64_t sw[2] = {K / 2, static_cast<uint64_t>(a.I) * (K / 2)};
-        const uint32_t bw[3] = {128, 64, 2};
-        ok = ok && encode(&maps[0], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.w, 3, dw, sw, bw,
-                          CU_TENSOR_MAP_SWIZZLE_128B);
         const uint64_t dp[3] = {K / 2, static_cast<uint64_t>(a.I), 2ull * a.E};
-        const uint32_t bp[3] = {static_cast<uint32_t>(kGroup * kBK / 2), 64, 2};
-        ok = ok && encode(&maps[5], CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w, 3, dp, sw, bp, CU_TENSOR_MAP_SWIZZLE_NONE);
+        const uint64_t sp[2] = {K / 2, static_cast<uint64_t>(a.I) * (K / 2)};
+        const uint32_t bp[3] = {static_cast<uint32_t>(kGroup * 128 / 2), 64, 2};
+        ok = ok && encode(&maps.wpf, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w, 3, dp, sp, bp, CU_TENSOR_MAP_SWIZZLE_NONE);
         if (sfa_tma) {
             const uint64_t ds[3] = {K / 32, static_cast<uint64_t>(a.I), 2ull * a.E};
             const uint64_t ss[2] = {K / 32, static_cast<uint64_t>(a.I) * (K / 32)};
             const uint32_t bs[3] = {16, 64, 2};
-            ok = ok && encode(&maps[6], CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_sf, 3, ds, ss, bs,
+            ok = ok && encode(&maps.wsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_sf, 3, ds, ss, bs,
                               CU_TENSOR_MAP_SWIZZLE_NONE);
         }
     } else {
-        const uint64_t dw[2] = {K, wrows};
-        const uint64_t sw[1] = {K / 2};
-        const uint32_t bw[2] = {128, 128};
-        ok = ok && encode(&maps[0], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.w, 2, dw, sw, bw,
-                          CU_TENSOR_MAP_SWIZZLE_128B);
         const uint64_t dp[2] = {K / 2, wrows};
-        const uint32_t bp[2] = {static_cast<uint32_t>(kGroup * kBK / 2), 128};
-        ok = ok && encode(&maps[5], CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w, 2, dp, sw, bp, CU_TENSOR_MAP_SWIZZLE_NONE);
+        const uint64_t sp[1] = {K / 2};
+        const uint32_t bp[2] = {static_cast<uint32_t>(kGroup * 128 / 2), 128};
+        ok = ok && encode(&maps.wpf, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w, 2, dp, sp, bp, CU_TENSOR_MAP_SWIZZLE_NONE);
         if (sfa_tma) {
             const uint64_t ds[2] = {K / 32, wrows};
             const uint64_t ss[1] = {K / 32};
             const uint32_t bs[2] = {16, 128};
-            ok = ok && encode(&maps[6], CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_sf, 2, ds, ss, bs,
+            ok = ok && encode(&maps.wsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_sf, 2, ds, ss, bs,
                               CU_TENSOR_MAP_SWIZZLE_NONE);
         }
     }
-    if (!sfa_tma) maps[6] = maps[5];   // not used on this path
-    for (int bi = 0; bi < 4; ++bi) {
-        const uint64_t db[2] = {K, static_cast<uint64_t>(a.S)};
-        const uint64_t sb[1] = {K};
-        const uint32_t bb[2] = {128, 16u << bi};
-        ok = ok && encode(&maps[1 + bi], CU_TENSOR_MAP_DATA_TYPE_UINT8, a.act, 2, db, sb, bb,
-                          CU_TENSOR_MAP_SWIZZLE_128B);
-    }
+    if (!sfa_tma) maps.wsf = maps.wpf;   // not used on this path
     {
-        const uint64_t da[2] = {static_cast<uint64_t>(S4), K / kBK};
+        const uint64_t da[2] = {static_cast<uint64_t>(S4), K / 128};
         const uint64_t sa[1] = {static_cast<uint64_t>(S4) * 4};
         const uint32_t ba[2] = {256, static_cast<uint32_t>(kGroup)};
-        ok = ok && encode(&maps[7], CU_TENSOR_MAP_DATA_TYPE_UINT32, a.act_sf, 2, da, sa, ba,
+        ok = ok && encode(&maps.asf, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.act_sf, 2, da, sa, ba,
                           CU_TENSOR_MAP_SWIZZLE_NONE);
     }
     if (!ok) return report(KT_ERR_CUDA, "tensor map encoding failed");
@@ -745,11 +1068,12 @@ kt_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
     const DebugSettings dbg = debug_settings();
     kp.wait_limit_ns = dbg.wait_limit_ns;
     kp.debug_flags = dbg.flags;
+    const int max_cluster = kGemmMaxCluster;
     cudaError_t e;
     switch (a.mode) {
-        case GemmEpilogue::Raw: e = launch_mode<0>(maps, kp, s); break;
-        case GemmEpilogue::SwiGLU: e = launch_mode<1>(maps, kp, s); break;
-        default: e = launch_mode<2>(maps, kp, s); break;
+        case GemmEpilogue::Raw: e = launch_mode<0>(maps, kp, max_cluster, s); break;
+        case GemmEpilogue::SwiGLU: e = launch_mode<1>(maps, kp, max_cluster, s); break;
+        default: e = launch_mode<2>(maps, kp, max_cluster, s); break;
     }
     return cuda_status(e);
 }

@@ -12,9 +12,12 @@
 namespace kt {
 
 // Token rows of one GEMM tile (the MMA N extent; two accumulator buffers of
-// this many columns fit in tensor memory next to the scale columns) and the
-// number of slots one permutation tile handles.
-constexpr int kTileTokens = 224;
+// this many columns fit in tensor memory next to the scale columns), the
+// most rows of one expert a tile covers (a tile starts at its first row
+// rounded down to a multiple of 8, so kChunkRows + 7 <= kTileTokens), and
+// the number of slots one permutation tile handles.
+constexpr int kTileTokens = 192;
+constexpr int kChunkRows = 176;
 constexpr int kPermTile = 1024;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
@@ -28,6 +31,10 @@ inline int perm_tiles(long long S) { return static_cast<int>((S + kPermTile - 1)
 // 32-element blocks 4ks..4ks+3 (block b in byte b % 4).  S4 = S rounded up to
 // a multiple of 4 keeps every row of the array 16-byte aligned for TMA.
 inline int sf_rows(long long S) { return static_cast<int>((S + 3) / 4 * 4); }
+
+// Activation code buffers (A1, A2) hold S rounded up to a multiple of 8 rows:
+// the GEMM loads token rows in whole groups of 8.
+inline long long act_rows(long long S) { return (S + 7) / 8 * 8; }
 
 // Workspace carving (offsets relative to the 256-byte aligned base).
 bool ws_layout(int T, int H, int I, int E, int k, kt_ws_layout* L);
@@ -43,7 +50,7 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int reno
                               cudaStream_t s);
 // Permutation of S = T*k slots: histogram -> scan -> stable scatter.
 // Writes expert_offsets [E+1], chunk_prefix [E+1] (token chunks of at most
-// kTileTokens rows per expert), perm [S], inv_perm [S]; hist is scratch of
+// kChunkRows rows per expert), perm [S], inv_perm [S]; hist is scratch of
 // perm_tiles(S) * E ints; err collects KT_DEVERR_BAD_EXPERT_ID.
 cudaError_t launch_permute(const int32_t* ids, long long S, int E, int32_t* hist, int32_t* expert_offsets,
                            int32_t* chunk_prefix, int32_t* perm, int32_t* inv_perm, int* err, cudaStream_t s);

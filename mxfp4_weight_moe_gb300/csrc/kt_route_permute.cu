@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ h
         }
     }
     const int cnt = (e < E) ? run : 0;
-    const int nch = (cnt + kTileTokens - 1) / kTileTokens;
+    const int nch = (cnt + kChunkRows - 1) / kChunkRows;
     int total_cnt, total_ch;
     const int off = block_exclusive_scan_1024(cnt, s_warp, &total_cnt);
     const int cpre = block_exclusive_scan_1024(nch, s_warp, &total_ch);
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(1024) chunk_prefix_kernel(const int32_t* __res
     __shared__ int s_warp[33];
     const int e = threadIdx.x;
     const int cnt = (e < E) ? offsets[e + 1] - offsets[e] : 0;
-    const int nch = cnt > 0 ? (cnt + kTileTokens - 1) / kTileTokens : 0;
+    const int nch = cnt > 0 ? (cnt + kChunkRows - 1) / kChunkRows : 0;
     int total;
     const int cpre = block_exclusive_scan_1024(nch, s_warp, &total);
     if (e < E) chunk_prefix[e] = cpre;
