@@ -46,6 +46,26 @@ METRIC = "MXFP4 fused-MoE layer tokens/s at 1 GB300; % of block-scaled roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0     # nominal dense ratio (4.5 / 2.25 PFLOP/s); mxf8f6f4 runs at the fp8 rate
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one FC1 launch
+# from an ncu capture of `python bench.py --warmup 3 --steps 1
+# --no-cpu-baseline` (profiles/mx_gemm_dsv4.md), keyed by workload and by the
+# SHA-256 of the GEMM source it was taken on: once the kernel changes, the
+# figure no longer applies and the bench line reports traffic null.
+GEMM_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mxfp4_weight_moe_gb300", "csrc", "kt_gemm_mx.cu")
+FC1_TRAFFIC = {
+    ("dsv4", "f97da29e27dc26f268fad3500dde7b332832df34548801221d6f3b00a933e948"): 2727207168 + 47077376,
+}
+
+
+def fc1_traffic(workload: str):
+    import hashlib
+
+    try:
+        sha = hashlib.sha256(open(GEMM_SRC, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return FC1_TRAFFIC.get((workload, sha))
+
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -350,7 +370,7 @@ def run_ours(args, cfg, world, rank, local):
         "gpu_launches": int(launches),
         "clocks": clocks,
         "roofline": {"bound": "hbm", "achieved": fc1_gbs, "peak": hbm, "unit": "GB/s", "frac": fc1_gbs / hbm,
-                     "traffic": None, "kernel": "mx_gemm_kernel<SwiGLU> (FC1)",
+                     "traffic": fc1_traffic(cfg.name), "kernel": "mx_gemm_kernel<SwiGLU> (FC1)",
                      "peak_source": f"{peak_src} hbm_gbs",
                      "algorithmic_bytes_per_launch": work["fc1_bytes"], "avg_launch_ms": fc1_ms},
         "layer_roofline": {"t_roof_ms": t_roof_ms, "frac": t_roof_ms / ms_per_step,
