@@ -99,7 +99,8 @@ constexpr int kStgBytes = kStgSFA + kStgSFB;  // one staging buffer
 constexpr int kStgBufs = 3;                   // staging ring: loads run kStgBufs - 1 groups ahead
 constexpr int kEpiBytes = 10240;              // FC1 exchange + transposes / FC2 transpose
 constexpr int kBarBytes = 512;
-constexpr int kSmemTotal = 1024 + kRing + 2 * kSfBytes + kStgBufs * kStgBytes + kEpiBytes + kBarBytes;
+constexpr int kTabBytes = 2 * (kMaxExperts + 1) * 4 + 8;   // chunk_prefix and expert_offsets, staged per CTA
+constexpr int kSmemTotal = 1024 + kRing + 2 * kSfBytes + kStgBufs * kStgBytes + kEpiBytes + kBarBytes + kTabBytes;
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kTileTokens;    // accumulator buffer b at column b * kAccCols
@@ -152,29 +153,37 @@ struct KParams {
     int debug_flags;
 };
 
+// The routing tables a CTA decodes its work units from, staged in shared
+// memory at kernel start (a binary search over global memory costs several
+// microseconds of dependent loads at every tile start).
+struct Tables {
+    const int32_t* cp;   // chunk_prefix [E+1]
+    const int32_t* eo;   // expert_offsets [E+1]
+};
+
 // Work unit u of a cluster -> (expert, feature-tile group, token chunk); the
 // CTA of cluster rank r takes feature tile group * cl + r.  Token chunks of
 // one (expert, feature-tile group) are adjacent so concurrent clusters share
 // weight tiles through L2.  chunk c of an expert with `cnt` rows split into
 // nc chunks covers rows [c*cnt/nc, (c+1)*cnt/nc).
-__device__ __forceinline__ void decode_tile(const KParams& p, int u, int rank, TileInfo& ti) {
+__device__ __forceinline__ void decode_tile(const KParams& p, const Tables& tb, int u, int rank, TileInfo& ti) {
     const int v = u / p.nfg;
     int lo = 1, hi = p.E;                   // first e' with chunk_prefix[e'] > v
     while (lo < hi) {
         const int mid = (lo + hi) >> 1;
-        if (__ldg(p.chunk_prefix + mid) > v) hi = mid;
+        if (tb.cp[mid] > v) hi = mid;
         else lo = mid + 1;
     }
     const int e = lo - 1;
-    const int c0 = __ldg(p.chunk_prefix + e);
-    const int nc = __ldg(p.chunk_prefix + e + 1) - c0;
+    const int c0 = tb.cp[e];
+    const int nc = tb.cp[e + 1] - c0;
     const int local = u - p.nfg * c0;
     ti.e = e;
     const int fg = local / nc;
     ti.f = fg * p.cl + rank;
     const int c = local - fg * nc;
-    const int off = __ldg(p.expert_offsets + e);
-    const int cnt = __ldg(p.expert_offsets + e + 1) - off;
+    const int off = tb.eo[e];
+    const int cnt = tb.eo[e + 1] - off;
     const int a = static_cast<int>(static_cast<long long>(c) * cnt / nc);
     const int b = static_cast<int>(static_cast<long long>(c + 1) * cnt / nc);
     const int r0 = off + a;
@@ -203,6 +212,10 @@ __device__ __forceinline__ void weight_coords(const KParams& p, const TileInfo& 
         z = 0;
     }
 }
+
+// SiLU with the fast reciprocal-based division (the division's 2-ulp error is
+// far below the MXFP8 step the result is quantised to next).
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -389,7 +402,10 @@ struct GroupCursor {
     int wy, wz;
     bool valid;
     int rank, stride;
-    __device__ __forceinline__ void start(const KParams& p, int total, int first, int rank_, int stride_) {
+    Tables tb;
+    __device__ __forceinline__ void start(const KParams& p, const Tables& tb_, int total, int first, int rank_,
+                                          int stride_) {
+        tb = tb_;
         u = first;
         rank = rank_;
         stride = stride_;
@@ -399,7 +415,7 @@ struct GroupCursor {
     __device__ __forceinline__ void load(const KParams& p, int total) {
         valid = u < total;
         if (valid) {
-            decode_tile(p, u, rank, ti);
+            decode_tile(p, tb, u, rank, ti);
             weight_coords<MODE>(p, ti, wy, wz);
         }
     }
@@ -424,6 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* epi = stg + kStgBufs * kStgBytes;
     uint8_t* bars = epi + kEpiBytes;
     const uint32_t bar_base = smem_u32(bars);
+    int32_t* s_cp = reinterpret_cast<int32_t*>(bars + kBarBytes);
+    int32_t* s_eo = s_cp + (kMaxExperts + 1);
+    const Tables tb{s_cp, s_eo};
     // barriers: full[S] empty[S] sf_full[2] sf_empty[2] stg[3] acc_full[2] acc_empty[2] drain
     const uint32_t full_base = bar_base;
     const uint32_t empty_base = bar_base + 8u * kSlots;
@@ -464,6 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         fence_proxy_async_smem();
     }
+    for (int i = threadIdx.x; i <= p.E; i += kThreads) {
+        s_cp[i] = __ldg(p.chunk_prefix + i);
+        s_eo[i] = __ldg(p.expert_offsets + i);
+    }
     if (warp == 1) {
         tc_alloc(smem_u32(tmem_slot), kTmemCols);
         tc_relinquish();
@@ -486,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int total = p.nfg * __ldg(p.chunk_prefix + p.E);   // work units of the grid's clusters
+    const int total = p.nfg * s_cp[p.E];   // work units of the grid's clusters
     const int nq = p.K / 128;                  // K quads per tile
     const int ngroups = (nq + kGroup - 1) / kGroup;
 
@@ -501,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             long long gi = 0;
             for (int u = first; u < total && ok; u += stride) {
                 TileInfo ti;
-                decode_tile(p, u, rank, ti);
+                decode_tile(p, tb, u, rank, ti);
                 int wy, wz;
                 weight_coords<MODE>(p, ti, wy, wz);
                 const uint32_t need = stage_bytes(ti);
@@ -552,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stg_tx = static_cast<uint32_t>(kStgSFB + (p.sfa_tma ? kStgSFA : 0));
         const int ksf = p.K / 32;
         GroupCursor<MODE> cur, ahead, pf;
-        cur.start(p, total, first, rank, stride);
+        cur.start(p, tb, total, first, rank, stride);
         ahead = cur;
         pf = cur;
         auto issue_staging = [&](const GroupCursor<MODE>& c, int buf) {
@@ -660,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true, issued = false;
             for (int u = first; u < total && ok; u += stride, ++it) {
                 TileInfo ti;
-                decode_tile(p, u, rank, ti);
+                decode_tile(p, tb, u, rank, ti);
                 const int ab = it & 1;
                 issued = true;
                 ok = wait(acc_empty(ab), ((acc_ph >> ab) & 1u) ^ 1u);
@@ -714,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (cl > 1) tc_commit_mc(empty_bar(slot), cl_mask);   // frees the stage in every CTA
                         else tc_commit(empty_bar(slot));
                     }
-                    wsync();
+                    // no warp sync here: the next barrier wait is a full-warp vote
                     if (group_end) {
                         sf_ph ^= 1u << sb;
                         sb ^= 1;
@@ -744,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int u = first; u < total && ok; u += stride, ++it) {
             TileInfo ti;
-            decode_tile(p, u, rank, ti);
+            decode_tile(p, tb, u, rank, ti);
             const int ab = it & 1;
             ok = __all_sync(0xffffffffu, mbar_wait(acc_full(ab), (acc_ph >> ab) & 1u, abort_flag, p.wait_limit_ns));
             if (!ok) break;
@@ -801,30 +824,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float* Y = reinterpret_cast<float*>(epi) + 1024 + pair * 512;   // up, columns 0-15
                     if (gate) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float g = __uint_as_float(v[16 + j]);
-                            X[j * 32 + lane] = g / (1.0f + __expf(-g));
-                        }
+                        for (int j = 0; j < 16; ++j) X[j * 32 + lane] = silu(__uint_as_float(v[16 + j]));
                     } else {
 #pragma unroll
                         for (int j = 0; j < 16; ++j) Y[j * 32 + lane] = __uint_as_float(v[j]);
                     }
                     named_bar_sync(1, 128);
                     uint8_t* my_bt = epi + 8192 + q * 512;   // [16 columns][32 features]
+                    // three independent passes (h, block amax, codes) so the 16 columns overlap
+                    float hv[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        hv[j] = gate ? silu(__uint_as_float(v[j])) * Y[j * 32 + lane]
+                                     : X[j * 32 + lane] * __uint_as_float(v[16 + j]);
+                    uint32_t am[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        am[j] = __reduce_max_sync(0xffffffffu, __float_as_uint(hv[j]) & 0x7FFFFFFFu);
                     uint8_t my_scale = 0;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        float hv;
-                        if (gate) {
-                            const float g = __uint_as_float(v[j]);
-                            hv = g / (1.0f + __expf(-g)) * Y[j * 32 + lane];
-                        } else {
-                            hv = X[j * 32 + lane] * __uint_as_float(v[16 + j]);
-                        }
-                        const uint32_t am = __reduce_max_sync(0xffffffffu, __float_as_uint(hv) & 0x7FFFFFFFu);
-                        const int X8 = mx_e4m3_block_exponent(am);
-                        my_bt[j * 32 + lane] = f32_to_e4m3_satfinite(hv * exp2_neg(X8));
-                        if (lane == j) my_scale = static_cast<uint8_t>(X8 + 127);
+                    for (int j = 0; j < 16; j += 2) {
+                        const int X0 = mx_e4m3_block_exponent(am[j]);
+                        const int X1 = mx_e4m3_block_exponent(am[j + 1]);
+                        const uint16_t c2 = f32x2_to_e4m3x2_satfinite(hv[j] * exp2_neg(X0), hv[j + 1] * exp2_neg(X1));
+                        my_bt[j * 32 + lane] = static_cast<uint8_t>(c2 & 0xFFu);
+                        my_bt[(j + 1) * 32 + lane] = static_cast<uint8_t>(c2 >> 8);
+                        if (lane == j) my_scale = static_cast<uint8_t>(X0 + 127);
+                        if (lane == j + 1) my_scale = static_cast<uint8_t>(X1 + 127);
                     }
                     __syncwarp();
                     const int col_t = c0 + (gate ? 0 : 16) + lane;
