@@ -53,7 +53,7 @@ FP8_OVER_BF16 = 2.0     # nominal dense ratio (4.5 / 2.25 PFLOP/s); mxf8f6f4 run
 # figure no longer applies and the bench line reports traffic null.
 GEMM_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mxfp4_weight_moe_gb300", "csrc", "kt_gemm_mx.cu")
 FC1_TRAFFIC = {
-    ("dsv4", "f97da29e27dc26f268fad3500dde7b332832df34548801221d6f3b00a933e948"): 2727207168 + 47077376,
+    ("dsv4", "f5a5fb3c560ea0a093580e2d346a66edb29f4c781df7eb1c7dceb7eccd682ec8"): 2688460288 + 47738368,
 }
 
 
