@@ -349,6 +349,30 @@ def run_ours(args, cfg, world, rank, local):
     e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e2e_steps, world, dev)
     assert torch.equal(out_host.view(torch.int16), out.cpu().view(torch.int16))
 
+    # ---- the same step captured once in a CUDA graph and replayed (device-resident inputs)
+    graph = None
+    try:
+        gstream = torch.cuda.Stream(dev)
+        gstream.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gstream):
+            ids_g, w_g, *_ = kt.route_permute(logits, k, out=route_out, workspace=ws_route, stream=gstream)
+            kt.forward(hidden, ids_g, w_g, *W, out=out, workspace=ws, stream=gstream)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        reps = max(3, min(args.steps, 50))
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        g_ms = max_over_ranks(ev0.elapsed_time(ev1) / reps, world, dev)
+        graph = {"value": T * world / (g_ms / 1e3), "unit": "tokens/s", "ms_per_step": g_ms, "replays": reps}
+        del g
+    except Exception as exc:  # noqa: BLE001 - reported, never fatal to the bench line
+        graph = {"error": f"{type(exc).__name__}: {exc}"[:200]}
+
     # ---- roofline of the dominant kernel (FC1 grouped GEMM) and of the layer
     work = algorithmic(cfg, touched)
     fc1_ms = prof["fc1"][0] / max(1, prof["fc1"][1])
@@ -368,6 +392,7 @@ def run_ours(args, cfg, world, rank, local):
                 "h2d_bytes_per_step": hidden.numel() * 2 + logits.numel() * 4,
                 "d2h_bytes_per_step": out.numel() * 2},
         "gpu_launches": int(launches),
+        "graph": graph,
         "clocks": clocks,
         "roofline": {"bound": "hbm", "achieved": fc1_gbs, "peak": hbm, "unit": "GB/s", "frac": fc1_gbs / hbm,
                      "traffic": fc1_traffic(cfg.name), "kernel": "mx_gemm_kernel<SwiGLU> (FC1)",
