@@ -43,13 +43,13 @@
 // so the MMA descriptor of quad q starts at the quad's first row with 1024 B
 // (weights) or kqs * 1024 B (tokens) between 8-row groups.
 //
-// Warp roles (256 threads, one CTA per SM, persistent over tiles):
+// Warp roles (288 threads, one CTA per SM, persistent over tiles):
 //   warp 0     weight producer (one lane): one 3-D (FC1: 4-D) TMA box with
 //              the stage's K quads of the weight tile.
 //   warp 1     MMA issuer: the whole warp follows the pipeline, one elected
 //              lane issues tcgen05.cp (scales -> tensor memory) and
 //              tcgen05.mma (4 per K quad) and commits to the barriers.
-//   warp 2     scale warp: per group of 4 K-quads it TMA-loads the weight
+//   warps 2, 8 scale warps (alternate groups): per group of 4 K-quads each TMA-loads the weight
 //              scales (16-byte rows of the plain [rows, K/32] layout) and the
 //              token scales (the K-step-major u32 layout the quantisers
 //              write) into a staging ring ahead of use, builds the 128x4
@@ -86,7 +86,7 @@ constexpr uint32_t kQuadWTx = 128 * 128 / 2;  // ... and its transaction bytes (
 #endif
 constexpr int kSmallN = KT_GEMM_SMALL_N;      // tiles of at most this many token rows use two-quad stages
 constexpr int kGemmMaxCluster = KT_GEMM_MAX_CLUSTER;
-constexpr int kRing = 176 * 1024;             // stage ring: weight tile + token tile per stage
+constexpr int kRing = 168 * 1024;             // stage ring: weight tile + token tile per stage
 constexpr int kMaxCluster = 4;
 static_assert(kGemmMaxCluster == 1 || kGemmMaxCluster == 2 || kGemmMaxCluster == 4, "cluster size");
 constexpr int kSlots = 4;                     // stages in flight at most (barrier pairs, tensor-memory scale slots)
@@ -96,12 +96,13 @@ constexpr int kSfBytes = kGroup * kSfQuad;    // one scale-block buffer (two of 
 constexpr int kStgSFA = 128 * 16;             // staging: 128 weight rows x 16 scale bytes
 constexpr int kStgSFB = kGroup * 256 * 4;     // staging: 4 quads x 256 token rows x u32
 constexpr int kStgBytes = kStgSFA + kStgSFB;  // one staging buffer
-constexpr int kStgBufs = 3;                   // staging ring: loads run kStgBufs - 1 groups ahead
+constexpr int kStgBufs = 4;                   // staging: two buffers per scale warp
+constexpr int kScaleWarp2 = 8;                // second scale warp (odd groups)
 constexpr int kEpiBytes = 10240;              // FC1 exchange + transposes / FC2 transpose
 constexpr int kBarBytes = 512;
 constexpr int kTabBytes = 2 * (kMaxExperts + 1) * 4 + 8;   // chunk_prefix and expert_offsets, staged per CTA
 constexpr int kSmemTotal = 1024 + kRing + 2 * kSfBytes + kStgBufs * kStgBytes + kEpiBytes + kBarBytes + kTabBytes;
-constexpr int kThreads = 256;
+constexpr int kThreads = 288;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kTileTokens;    // accumulator buffer b at column b * kAccCols
 constexpr uint32_t kTmemSF = 2 * kAccCols;    // scale columns after both accumulators
@@ -568,16 +569,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *abort_flag = 1;
             }
         }
-    } else if (warp == 2) {
-        // ------------------------------------------------------------ scale warp
+    } else if (warp == 2 || warp == kScaleWarp2) {
+        // ------------------------------------------------------------ scale warps
+        // Warp 2 builds the even groups, warp 8 the odd ones; group g uses
+        // scale-block buffer g & 1, so each warp owns one buffer and two
+        // staging buffers.  (One warp alone paced the pipeline on GB300.)
+        const int sw = warp == 2 ? 0 : 1;
         uint32_t stg_ph = 0u, sfe_ph = 0u;   // one parity bit per buffer
         bool ok = true;
         const uint32_t stg_tx = static_cast<uint32_t>(kStgSFB + (p.sfa_tma ? kStgSFA : 0));
         const int ksf = p.K / 32;
         GroupCursor<MODE> cur, ahead, pf;
         cur.start(p, tb, total, first, rank, stride);
+        if (sw) cur.advance(p, total, ngroups);
         ahead = cur;
         pf = cur;
+        auto advance2 = [&](GroupCursor<MODE>& c) {
+            c.advance(p, total, ngroups);
+            c.advance(p, total, ngroups);
+        };
         auto issue_staging = [&](const GroupCursor<MODE>& c, int buf) {
             if (lane == 0 && c.valid) {
                 const uint32_t dst = smem_u32(stg + buf * kStgBytes);
@@ -590,23 +600,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto prefetch_group = [&](const GroupCursor<MODE>& c) {
             if (lane == 0 && c.valid) prefetch_weight_box<MODE>(&maps.wpf, c.g * (kGroup * 128 / 2), c.wy, c.wz);
         };
-        for (int i = 0; i < kPrefetchGroups; ++i) {
+        for (int i = 0; i < kPrefetchGroups; ++i) {   // this warp's next groups
             prefetch_group(pf);
-            pf.advance(p, total, ngroups);
+            advance2(pf);
         }
-        for (int i = 0; i < kStgBufs - 1; ++i) {   // staging for the first groups
-            issue_staging(ahead, i);
-            ahead.advance(p, total, ngroups);
-        }
-        int gidx = 0;
+        issue_staging(ahead, 2 * sw);   // staging for this warp's first group
+        advance2(ahead);
+        int lidx = 0;                   // this warp's groups so far (global group 2 * lidx + sw)
         while (cur.valid && ok) {
-            const int sbuf = gidx % kStgBufs;     // staging buffer of this group
-            const int fbuf = gidx & 1;            // scale-block buffer of this group
-            __syncwarp();                         // every lane is done with the buffer refilled next
-            issue_staging(ahead, (gidx + kStgBufs - 1) % kStgBufs);
-            ahead.advance(p, total, ngroups);
+            const int sbuf = 2 * sw + (lidx & 1);   // staging buffer of this group
+            const int fbuf = sw;                    // scale-block buffer of this group
+            __syncwarp();                           // every lane is done with the buffer refilled next
+            issue_staging(ahead, 2 * sw + ((lidx + 1) & 1));
+            advance2(ahead);
             prefetch_group(pf);
-            pf.advance(p, total, ngroups);
+            advance2(pf);
             ok = __all_sync(0xffffffffu, mbar_wait(stg_bar(sbuf), (stg_ph >> sbuf) & 1u, abort_flag,
                                                    p.wait_limit_ns));
             if (!ok) break;
@@ -620,15 +628,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nkk = min(kGroup, nq - kq0);
             const int natoms = ti.nmma > 128 ? 2 : 1;
             const int lo = ti.lead, hi = ti.lead + ti.nvalid;
-            for (int kk = 0; kk < nkk; ++kk) {
-                uint8_t* blk = sfo + kk * kSfQuad;
-                // weight scales: tile row r -> byte (r%32)*16 + (r/32)*4 of the 512-byte block
-                if (p.sfa_tma) {
-                    uint32_t w4[4];
+            // weight scales: staging row r holds the 16 scale bytes of the group (word kk = quad kk); one
+            // 16-byte load per row serves all four quads (consecutive rows per lane: no bank conflicts)
+            uint4 wrow[4];
+            if (p.sfa_tma) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        w4[i] = *reinterpret_cast<const uint32_t*>(sb + (lane + 32 * i) * 16 + kk * 4);
-                    *reinterpret_cast<uint4*>(blk + lane * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                for (int i = 0; i < 4; ++i) wrow[i] = *reinterpret_cast<const uint4*>(sb + (lane + 32 * i) * 16);
+            }
+#pragma unroll
+            for (int kk = 0; kk < kGroup; ++kk) {
+                if (kk >= nkk) break;
+                uint8_t* blk = sfo + kk * kSfQuad;
+                // tile row r -> byte (r%32)*16 + (r/32)*4 of the 512-byte block
+                if (p.sfa_tma) {
+                    auto word = [&](const uint4& v) { return kk == 0 ? v.x : kk == 1 ? v.y : kk == 2 ? v.z : v.w; };
+                    *reinterpret_cast<uint4*>(blk + lane * 16) =
+                        make_uint4(word(wrow[0]), word(wrow[1]), word(wrow[2]), word(wrow[3]));
                 } else {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -659,8 +674,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             else cp_async_arrive_noinc(sf_full(fbuf));
             stg_ph ^= 1u << sbuf;
             sfe_ph ^= 1u << fbuf;
-            ++gidx;
-            cur.advance(p, total, ngroups);
+            ++lidx;
+            advance2(cur);
         }
         if (!ok) {
             if (lane == 0) set_error(p.err, KT_DEVERR_TIMEOUT_LOAD);
