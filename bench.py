@@ -53,7 +53,7 @@ FP8_OVER_BF16 = 2.0     # nominal dense ratio (4.5 / 2.25 PFLOP/s); mxf8f6f4 run
 # figure no longer applies and the bench line reports traffic null.
 GEMM_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mxfp4_weight_moe_gb300", "csrc", "kt_gemm_mx.cu")
 FC1_TRAFFIC = {
-    ("dsv4", "f5a5fb3c560ea0a093580e2d346a66edb29f4c781df7eb1c7dceb7eccd682ec8"): 2688460288 + 47738368,
+    ("dsv4", "e33d04919b685469c08f8d51f516ae67e8d806b8c8f86134ffe1b760c60fc624"): 2758080256 + 47421440,
 }
 
 
