@@ -27,16 +27,25 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
     __syncwarp();
     const int nblk = H >> 5;
     const uint16_t* row = hidden + static_cast<size_t>(t) * H;
+    // two 32-element blocks per lane per pass, both loaded before either is converted
+    uint4 nxt[4];
+    if (lane < nblk) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) nxt[i] = __ldcs(reinterpret_cast<const uint4*>(row + lane * 32) + i);
+    }
     for (int b = lane; b < nblk; b += 32) {
-        const uint4* src = reinterpret_cast<const uint4*>(row + b * 32);
         uint32_t wv[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint4 q = src[i];
+            const uint4 q = nxt[i];
             wv[4 * i + 0] = q.x;
             wv[4 * i + 1] = q.y;
             wv[4 * i + 2] = q.z;
             wv[4 * i + 3] = q.w;
+        }
+        if (b + 32 < nblk) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) nxt[i] = __ldcs(reinterpret_cast<const uint4*>(row + (b + 32) * 32) + i);
         }
         float x[32];
         uint32_t amax = 0;
@@ -120,15 +129,28 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const int e = ids[static_cast<size_t>(t) * k + j];
-            if (e < 0 || e >= E) continue;
-            const uint4 q = *reinterpret_cast<const uint4*>(y + (static_cast<size_t>(t) * k + j) * H + h8 * 8);
-            const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+        // slots in order (the sum order is fixed); loads of four slots are in flight together
+        for (int j0 = 0; j0 < k; j0 += 4) {
+            uint4 q[4];
+            bool use[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] += __uint_as_float(wv[i] << 16);
-                acc[2 * i + 1] += __uint_as_float(wv[i] & 0xFFFF0000u);
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u;
+                int e = -1;
+                if (j < k) e = __ldg(ids + static_cast<size_t>(t) * k + j);
+                use[u] = e >= 0 && e < E;
+                q[u] = use[u] ? __ldcs(reinterpret_cast<const uint4*>(y + (static_cast<size_t>(t) * k + j) * H + h8 * 8))
+                              : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (!use[u]) continue;
+                const uint32_t wv[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] += __uint_as_float(wv[i] << 16);
+                    acc[2 * i + 1] += __uint_as_float(wv[i] & 0xFFFF0000u);
+                }
             }
         }
         uint32_t o[4];

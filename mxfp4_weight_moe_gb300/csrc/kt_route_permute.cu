@@ -21,6 +21,9 @@ namespace kt {
 // arg-max (value descending, index ascending) pick the experts in order.
 // Weights are exp(l_j - l_max) / sum in fp64 (the difference of two f32
 // logits is exact in fp64), then rounded to f32.
+// EPL = expert slots per lane, a power of two >= ceil(E / 32): the candidate
+// scans run over EPL slots, not 32 (E = 256 needs 8).
+template <int EPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                          int renormalize, int32_t* __restrict__ ids,
                                                          float* __restrict__ w) {
@@ -28,12 +31,11 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
     const float* row = logits + static_cast<size_t>(t) * E;
-    const int epl = (E + 31) >> 5;
-    float v[32];
+    float v[EPL];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
-        v[i] = (i < epl && e < E) ? row[e] : -INFINITY;
+        v[i] = (e < E) ? row[e] : -INFINITY;
     }
     constexpr int kNone = 0x7fffffff;
     uint32_t taken = 0;
@@ -43,9 +45,9 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
         float bv = -INFINITY;
         int bi = kNone;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
-            if (i < epl && e < E && !((taken >> i) & 1u)) {
+            if (e < E && !((taken >> i) & 1u)) {
                 if (bi == kNone || v[i] > bv) {
                     bv = v[i];
                     bi = e;
@@ -74,9 +76,9 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
         part = ex;
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
-            if (i < epl && e < E) part += exp(static_cast<double>(v[i]) - lmax);
+            if (e < E) part += exp(static_cast<double>(v[i]) - lmax);
         }
     }
 #pragma unroll
@@ -91,7 +93,13 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int reno
                               cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     const int blocks = (T + 7) / 8;
-    route_topk_kernel<<<blocks, 256, 0, s>>>(logits, T, E, k, renormalize, ids, w);
+    const int epl = (E + 31) / 32;   // E <= kMaxExperts = 1024 keeps this <= 32
+    if (epl <= 1) route_topk_kernel<1><<<blocks, 256, 0, s>>>(logits, T, E, k, renormalize, ids, w);
+    else if (epl <= 2) route_topk_kernel<2><<<blocks, 256, 0, s>>>(logits, T, E, k, renormalize, ids, w);
+    else if (epl <= 4) route_topk_kernel<4><<<blocks, 256, 0, s>>>(logits, T, E, k, renormalize, ids, w);
+    else if (epl <= 8) route_topk_kernel<8><<<blocks, 256, 0, s>>>(logits, T, E, k, renormalize, ids, w);
+    else if (epl <= 16) route_topk_kernel<16><<<blocks, 256, 0, s>>>(logits, T, E, k, renormalize, ids, w);
+    else route_topk_kernel<32><<<blocks, 256, 0, s>>>(logits, T, E, k, renormalize, ids, w);
     count_launches(1);
     return cudaGetLastError();
 }
