@@ -53,7 +53,7 @@ FP8_OVER_BF16 = 2.0     # nominal dense ratio (4.5 / 2.25 PFLOP/s); mxf8f6f4 run
 # figure no longer applies and the bench line reports traffic null.
 GEMM_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mxfp4_weight_moe_gb300", "csrc", "kt_gemm_mx.cu")
 FC1_TRAFFIC = {
-    ("dsv4", "e33d04919b685469c08f8d51f516ae67e8d806b8c8f86134ffe1b760c60fc624"): 2758080256 + 47421440,
+    ("dsv4", "6503a929a318ea51de4dc290a3e2d15dba2f2f1e9bf139d7faa034d921d4a0ac"): 2767272192 + 47961088,
 }
 
 

@@ -86,7 +86,7 @@ constexpr uint32_t kQuadWTx = 128 * 128 / 2;  // ... and its transaction bytes (
 #endif
 constexpr int kSmallN = KT_GEMM_SMALL_N;      // tiles of at most this many token rows use two-quad stages
 constexpr int kGemmMaxCluster = KT_GEMM_MAX_CLUSTER;
-constexpr int kRing = 168 * 1024;             // stage ring: weight tile + token tile per stage
+constexpr int kRing = 176 * 1024;             // stage ring: weight tile + token tile per stage
 constexpr int kMaxCluster = 4;
 static_assert(kGemmMaxCluster == 1 || kGemmMaxCluster == 2 || kGemmMaxCluster == 4, "cluster size");
 constexpr int kSlots = 4;                     // stages in flight at most (barrier pairs, tensor-memory scale slots)
@@ -94,13 +94,13 @@ constexpr int kGroup = 4;                     // K quads per scale group
 constexpr int kSfQuad = 512 + 1024;           // per quad: weight scale block + up to 2 token blocks
 constexpr int kSfBytes = kGroup * kSfQuad;    // one scale-block buffer (two of them)
 constexpr int kStgSFA = 128 * 16;             // staging: 128 weight rows x 16 scale bytes
-constexpr int kStgSFB = kGroup * 256 * 4;     // staging: 4 quads x 256 token rows x u32
+constexpr int kStgSFB = kGroup * kTileTokens * 4;   // staging: 4 quads x tile token rows x u32
 constexpr int kStgBytes = kStgSFA + kStgSFB;  // one staging buffer
 constexpr int kStgBufs = 4;                   // staging: two buffers per scale warp
 constexpr int kScaleWarp2 = 8;                // second scale warp (odd groups)
 constexpr int kEpiBytes = 10240;              // FC1 exchange + transposes / FC2 transpose
 constexpr int kBarBytes = 512;
-constexpr int kTabBytes = 2 * (kMaxExperts + 1) * 4 + 8;   // chunk_prefix and expert_offsets, staged per CTA
+constexpr int kTabBytes = (kMaxExperts + 1) * 4 + 8;   // chunk_prefix, staged per CTA
 constexpr int kSmemTotal = 1024 + kRing + 2 * kSfBytes + kStgBufs * kStgBytes + kEpiBytes + kBarBytes + kTabBytes;
 constexpr int kThreads = 288;
 constexpr uint32_t kTmemCols = 512;
@@ -154,12 +154,13 @@ struct KParams {
     int debug_flags;
 };
 
-// The routing tables a CTA decodes its work units from, staged in shared
-// memory at kernel start (a binary search over global memory costs several
-// microseconds of dependent loads at every tile start).
+// The routing tables a CTA decodes its work units from.  chunk_prefix is
+// staged in shared memory at kernel start (a binary search over global
+// memory costs several microseconds of dependent loads at every tile
+// start); expert_offsets stays in global memory (two loads per tile).
 struct Tables {
-    const int32_t* cp;   // chunk_prefix [E+1]
-    const int32_t* eo;   // expert_offsets [E+1]
+    const int32_t* cp;   // chunk_prefix [E+1], shared memory
+    const int32_t* eo;   // expert_offsets [E+1], global memory
 };
 
 // Work unit u of a cluster -> (expert, feature-tile group, token chunk); the
@@ -183,8 +184,8 @@ __device__ __forceinline__ void decode_tile(const KParams& p, const Tables& tb, 
     const int fg = local / nc;
     ti.f = fg * p.cl + rank;
     const int c = local - fg * nc;
-    const int off = tb.eo[e];
-    const int cnt = tb.eo[e + 1] - off;
+    const int off = __ldg(tb.eo + e);
+    const int cnt = __ldg(tb.eo + e + 1) - off;
     const int a = static_cast<int>(static_cast<long long>(c) * cnt / nc);
     const int b = static_cast<int>(static_cast<long long>(c + 1) * cnt / nc);
     const int r0 = off + a;
@@ -442,8 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* bars = epi + kEpiBytes;
     const uint32_t bar_base = smem_u32(bars);
     int32_t* s_cp = reinterpret_cast<int32_t*>(bars + kBarBytes);
-    int32_t* s_eo = s_cp + (kMaxExperts + 1);
-    const Tables tb{s_cp, s_eo};
+    const Tables tb{s_cp, p.expert_offsets};
     // barriers: full[S] empty[S] sf_full[2] sf_empty[2] stg[3] acc_full[2] acc_empty[2] drain
     const uint32_t full_base = bar_base;
     const uint32_t empty_base = bar_base + 8u * kSlots;
@@ -486,7 +486,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = threadIdx.x; i <= p.E; i += kThreads) {
         s_cp[i] = __ldg(p.chunk_prefix + i);
-        s_eo[i] = __ldg(p.expert_offsets + i);
     }
     if (warp == 1) {
         tc_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -657,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 // token scales from the K-step-major staging rows (tile column t = row r_al + t)
-                const uint32_t* arow = reinterpret_cast<const uint32_t*>(sb + kStgSFA) + kk * 256;
+                const uint32_t* arow = reinterpret_cast<const uint32_t*>(sb + kStgSFA) + kk * kTileTokens;
                 for (int a = 0; a < natoms; ++a) {
                     uint32_t t4[4];
 #pragma unroll
@@ -736,16 +735,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t sF = smem_u32(sfbuf + sb * kSfBytes + kk * kSfQuad);
                             const uint32_t t_sfa = tmem + kTmemSF + slot * kSfSlotCols + q * 12;
                             const uint32_t t_sfb = t_sfa + 4;
-                            tc_cp_32x128b_warpx4(t_sfa, sdesc_sf_block(sF));
-                            tc_cp_32x128b_warpx4(t_sfb, sdesc_sf_block(sF + 512));
-                            if (ti.nmma > 128) tc_cp_32x128b_warpx4(t_sfb + 4, sdesc_sf_block(sF + 1024));
+                            const uint64_t dF = sdesc_sf_block(sF);
+                            tc_cp_32x128b_warpx4(t_sfa, dF);
+                            tc_cp_32x128b_warpx4(t_sfb, dF + (512 >> 4));
+                            if (ti.nmma > 128) tc_cp_32x128b_warpx4(t_sfb + 4, dF + (1024 >> 4));
+                            // descriptors built once per quad; each 32-byte K step adds 2 to
+                            // the start-address field (bits 0-13, address >> 4; no carry out
+                            // below 256 KB of shared memory)
+                            const uint64_t dA = sdesc_sw128_sbo(sA, 1024);
+                            const uint64_t dB = sdesc_sw128_sbo(sB, tok_sbo);
+                            const uint32_t acc0 = (kq0 + q) != 0 ? 1u : 0u;
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 const uint32_t idesc =
                                     idesc0 | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
-                                tc_mma_mxf8f6f4(d_tmem, sdesc_sw128_sbo(sA + 32 * j, 1024),
-                                                sdesc_sw128_sbo(sB + 32 * j, tok_sbo), idesc, t_sfa, t_sfb,
-                                                ((kq0 + q) | j) != 0 ? 1u : 0u);
+                                tc_mma_mxf8f6f4(d_tmem, dA + static_cast<uint64_t>(2 * j), dB + static_cast<uint64_t>(2 * j),
+                                                idesc, t_sfa, t_sfb, j != 0 ? 1u : acc0);
                             }
                         }
                         if (group_end) tc_commit(sf_empty(sb));
@@ -1081,7 +1086,7 @@ kt_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
     {
         const uint64_t da[2] = {static_cast<uint64_t>(S4), K / 128};
         const uint64_t sa[1] = {static_cast<uint64_t>(S4) * 4};
-        const uint32_t ba[2] = {256, static_cast<uint32_t>(kGroup)};
+        const uint32_t ba[2] = {static_cast<uint32_t>(kTileTokens), static_cast<uint32_t>(kGroup)};
         ok = ok && encode(&maps.asf, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.act_sf, 2, da, sa, ba,
                           CU_TENSOR_MAP_SWIZZLE_NONE);
     }
