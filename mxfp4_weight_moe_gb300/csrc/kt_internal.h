@@ -48,7 +48,8 @@ bool route_ws_layout(int T, int E, int k, RouteWs* L);
 // All return cudaSuccess or the launch error; none synchronises.
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renormalize, int32_t* ids, float* w,
                               cudaStream_t s);
-// Permutation of S = T*k slots: histogram -> scan -> stable scatter.
+// Permutation of S = T*k slots: histogram -> scan -> stable scatter (one
+// single-block launch up to 2048 slots, three launches above).
 // Writes expert_offsets [E+1], chunk_prefix [E+1] (token chunks of at most
 // kChunkRows rows per expert), perm [S], inv_perm [S]; hist is scratch of
 // perm_tiles(S) * E ints; err collects KT_DEVERR_BAD_EXPERT_ID.
