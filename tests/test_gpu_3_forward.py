@@ -105,6 +105,17 @@ def test_forward_small_configs(name):
 
 
 @pytest.mark.parametrize("shape", [
+    (25, 384, 2, 2, 640),      # 25 rows per expert (32-row tiles with a lead), K = 3 and 5 quads, FC2 unclustered
+    (7, 256, 5, 3, 128),       # K = 2 and 1 quads (a 256-K stage over a single quad)
+    (24, 512, 3, 3, 256),      # k = E: every expert gets every token
+])
+def test_forward_decode_shapes(shape):
+    """Decode-sized ragged layers (T <= 25)."""
+    T, H, E, k, I = shape
+    _check_case(*_inputs(T=T, H=H, E=E, k=k, I=I, seed=11))
+
+
+@pytest.mark.parametrize("shape", [
     (37, 384, 5, 2, 384),      # ragged: 3 K steps, 6 FC1 feature tiles, 3 FC2 tiles
     (600, 256, 4, 1, 128),     # ~150 tokens per expert: token chunks, odd tails
     (300, 128, 3, 3, 256),     # k = E, every expert gets every token (2 chunks of 150)
