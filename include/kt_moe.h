@@ -255,6 +255,14 @@ uint64_t kt_moe_kernel_launches(void);
  */
 kt_status kt_moe_profile_enable(int enable);
 kt_status kt_moe_profile_read(double* stage_ms, int* calls);
+/*
+ * As kt_moe_profile_enable, recording only the stages whose bit
+ * (1 << KT_STAGE_*) is set in stage_mask; 0 disables.  Each recorded stage
+ * adds two event records to the stream, so a caller timing whole steps can
+ * record just the stage it needs.  Bits at or above KT_NUM_STAGES:
+ * KT_ERR_INVALID_ARG.
+ */
+kt_status kt_moe_profile_enable_stages(uint32_t stage_mask);
 
 /*
  * Test hook for the device-side failure path.  wait_limit_us bounds every

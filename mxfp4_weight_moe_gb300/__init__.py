@@ -73,6 +73,7 @@ _SIGNATURES = {
     "kt_moe_profile_enable": ([_I], _I),
     "kt_moe_profile_read": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)], _I),
     "kt_moe_debug_configure": ([ctypes.c_uint64, _I], _I),
+    "kt_moe_profile_enable_stages": ([ctypes.c_uint32], _I),
     "kt_moe_route_permute_noalloc": ([_VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP], _I),
 }
 
@@ -269,9 +270,17 @@ def kernel_launches() -> int:
     return int(lib().kt_moe_kernel_launches())
 
 
-def profile_enable(enable: bool = True):
-    """Start (or stop) recording per-stage CUDA events; discards old records."""
-    _check(lib().kt_moe_profile_enable(int(bool(enable))), "kt_moe_profile_enable")
+def profile_enable(enable: bool = True, stages=None):
+    """Start (or stop) recording per-stage CUDA events; discards old records.
+    `stages` (names from STAGES) limits the recording to those stages."""
+    if stages is None:
+        _check(lib().kt_moe_profile_enable(int(bool(enable))), "kt_moe_profile_enable")
+        return
+    mask = 0
+    if enable:
+        for name in stages:
+            mask |= 1 << STAGES.index(name)
+    _check(lib().kt_moe_profile_enable_stages(mask), "kt_moe_profile_enable_stages")
 
 
 def debug_configure(wait_limit_us: int = 0, flags: int = 0):

@@ -26,6 +26,7 @@ struct StageRecord {
 };
 
 static bool g_prof_on = false;
+static uint32_t g_prof_mask = 0;   // bit s: record stage s
 static std::vector<StageRecord> g_records;
 static std::vector<cudaEvent_t> g_pool;
 static size_t g_pool_used = 0;
@@ -40,7 +41,7 @@ static cudaEvent_t take_event() {
 }
 
 StageTimer::StageTimer(int stage, cudaStream_t s) : stage_(stage), s_(s), end_(nullptr) {
-    if (!g_prof_on) return;
+    if (!g_prof_on || !((g_prof_mask >> stage) & 1u)) return;
     cudaEvent_t b = take_event();
     end_ = take_event();
     if (!b || !end_) {
@@ -68,11 +69,17 @@ kt_status kt_moe_debug_configure(uint64_t wait_limit_us, int flags) {
     return KT_OK;
 }
 
-kt_status kt_moe_profile_enable(int enable) {
-    kt::g_prof_on = enable != 0;
+kt_status kt_moe_profile_enable_stages(uint32_t stage_mask) {
+    if (stage_mask >> KT_NUM_STAGES) return KT_ERR_INVALID_ARG;
+    kt::g_prof_on = stage_mask != 0;
+    kt::g_prof_mask = stage_mask;
     kt::g_records.clear();
     kt::g_pool_used = 0;
     return KT_OK;
+}
+
+kt_status kt_moe_profile_enable(int enable) {
+    return kt_moe_profile_enable_stages(enable ? (1u << KT_NUM_STAGES) - 1u : 0u);
 }
 
 kt_status kt_moe_profile_read(double* stage_ms, int* calls) {

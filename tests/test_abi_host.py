@@ -190,3 +190,8 @@ def test_debug_configure_rejects_unknown_flags():
     with pytest.raises(kt.KTError):
         kt.debug_configure(0, 0x80)
     kt.debug_configure()
+
+
+def test_profile_stage_mask_rejects_unknown_stages():
+    assert kt.lib().kt_moe_profile_enable_stages(1 << len(kt.STAGES)) == -1   # KT_ERR_INVALID_ARG
+    assert kt.lib().kt_moe_profile_enable_stages(0) == 0

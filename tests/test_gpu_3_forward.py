@@ -156,6 +156,20 @@ def test_forward_zero_weights_give_zero():
     assert torch.all(out.float() == 0)
 
 
+def test_profile_records_only_the_selected_stages():
+    hidden, ids, w, W = _inputs(T=32, H=512, E=4, k=2, I=256, seed=3)
+    ids_t, w_t = torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda()
+    kt.profile_enable(True, stages=("fc1",))
+    try:
+        kt.forward(hidden, ids_t, w_t, *W)
+        kt.forward(hidden, ids_t, w_t, *W)
+        prof = kt.profile_read()
+    finally:
+        kt.profile_enable(False)
+    assert prof["fc1"][1] == 2 and prof["fc1"][0] > 0
+    assert all(n == 0 for name, (_, n) in prof.items() if name != "fc1")
+
+
 def test_forward_is_deterministic():
     hidden, ids, w, W = _inputs("small_T32")
     ids_t, w_t = torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda()
