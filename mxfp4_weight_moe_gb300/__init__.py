@@ -87,6 +87,8 @@ STAGES = ("route", "permute", "quant", "fc1", "fc2", "combine")
 def lib(build_if_missing: bool = True):
     """The loaded C library (built in-tree on first use if absent)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             path = build_ext.build() if build_if_missing else build_ext.LIB_PATH
@@ -113,12 +115,29 @@ def _check(status: int, what: str):
 
 
 def _ptr(t: torch.Tensor | None):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()   # the signatures declare c_void_p
 
 
 def _stream_ptr(stream, device):
     s = torch.cuda.current_stream(device) if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    return s.cuda_stream
+
+
+class _on_device:
+    """Make `dev` the current CUDA device for a call (a no-op when it already is)."""
+    __slots__ = ("idx", "prev")
+
+    def __init__(self, dev: torch.device):
+        self.idx = dev.index
+
+    def __enter__(self):
+        self.prev = torch.cuda.current_device()
+        if self.idx is not None and self.idx != self.prev:
+            torch.cuda.set_device(self.idx)
+
+    def __exit__(self, *exc):
+        if self.idx is not None and self.idx != self.prev:
+            torch.cuda.set_device(self.prev)
 
 
 def _need(t: torch.Tensor, name: str, dtype, ndim: int, device=None):
@@ -197,13 +216,13 @@ def route_permute(logits: torch.Tensor, k: int, renormalize: bool = True, stream
                torch.empty(E + 1, dtype=torch.int32, device=dev), torch.empty(T * k, dtype=torch.int32, device=dev),
                torch.empty(T * k, dtype=torch.int32, device=dev))
     ids, w, offsets, perm, inv = out
-    nbytes = int(lib().kt_moe_route_workspace_bytes(T, E, k))
-    if nbytes == 0 and T > 0:
-        _check(lib().kt_moe_route_permute(None, T, E, k, 1, None, None, None, None, None, None, 0, None),
-               "kt_moe_route_permute")
     if workspace is None:
+        nbytes = int(lib().kt_moe_route_workspace_bytes(T, E, k))
+        if nbytes == 0 and T > 0:   # invalid shape: let the library report it
+            _check(lib().kt_moe_route_permute(None, T, E, k, 1, None, None, None, None, None, None, 0, None),
+                   "kt_moe_route_permute")
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         _check(lib().kt_moe_route_permute(_ptr(logits), T, E, k, int(bool(renormalize)), _ptr(ids), _ptr(w),
                                           _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(workspace), workspace.numel(),
                                           _stream_ptr(stream, dev)), "kt_moe_route_permute")
@@ -230,10 +249,9 @@ def forward(hidden: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, 
     if out is None:
         out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     _need(out, "out", torch.bfloat16, 2, dev)
-    nbytes = workspace_bytes(T, H, I, E, k)
-    if workspace is None:
-        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
-    with torch.cuda.device(dev):
+    if workspace is None:   # a caller's workspace is size-checked by the library
+        workspace = torch.empty(max(workspace_bytes(T, H, I, E, k), 1), dtype=torch.uint8, device=dev)
+    with _on_device(dev):
         _check(lib().kt_mxfp4_moe_forward(_ptr(hidden), T, H, _ptr(topk_ids), _ptr(topk_w), k, _ptr(w13),
                                           _ptr(w13_sf), _ptr(w2), _ptr(w2_sf), E, I, _ptr(out), _ptr(workspace),
                                           workspace.numel(), _stream_ptr(stream, dev)), "kt_mxfp4_moe_forward")

@@ -484,6 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         fence_proxy_async_smem();
     }
+    // the first global-memory access: the previous kernel in the stream has completed
+    griddep_wait();
+    griddep_launch_dependents();
     for (int i = threadIdx.x; i <= p.E; i += kThreads) {
         s_cp[i] = __ldg(p.chunk_prefix + i);
     }
@@ -1009,13 +1012,17 @@ static cudaError_t launch_mode(const GemmMaps& maps, KParams kp, int max_cluster
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemTotal;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(c);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    // programmatic stream serialization: the CTAs may start (barriers, tensor
+    // memory) while the previous kernel finishes; they wait before reading
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(c);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = c > 1 ? 1 : 0;
+    cfg.numAttrs = c > 1 ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, mx_gemm_kernel<MODE>, maps, kp);
     count_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();

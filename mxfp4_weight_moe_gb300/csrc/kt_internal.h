@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -43,6 +44,26 @@ struct RouteWs {
     size_t err, hist, chunk_prefix, total;
 };
 bool route_ws_layout(int T, int E, int k, RouteWs* L);
+
+// Launch with programmatic stream serialization: the kernel may begin while
+// its predecessor in the stream runs, and waits for it (griddep_wait) before
+// touching global memory.  Used for every kernel of the routing and forward
+// paths.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                  Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ------------------------------------------------------------- launchers
 // All return cudaSuccess or the launch error; none synchronises.

@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
                                                             const int32_t* __restrict__ inv_perm,
                                                             uint8_t* __restrict__ a1, uint8_t* __restrict__ a1_sf,
                                                             int S4) {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ int s_dst[8][kMaxTopK];
     const int wib = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -80,9 +82,10 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
 cudaError_t launch_quant_scatter(const uint16_t* hidden, int T, int H, int k, const int32_t* inv_perm, uint8_t* a1,
                                  uint8_t* a1_sf, int S4, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    quant_scatter_kernel<<<(T + 7) / 8, 256, 0, s>>>(hidden, T, H, k, inv_perm, a1, a1_sf, S4);
+    const cudaError_t e = launch_chained(quant_scatter_kernel, dim3((T + 7) / 8), dim3(256), 0, s, hidden, T, H, k,
+                                         inv_perm, a1, a1_sf, S4);
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // Plain [S, K/32] scale bytes -> K-step-major u32 [K/128][S4] (one thread per
@@ -120,6 +123,8 @@ cudaError_t launch_sf_to_kstep_major(const uint8_t* plain, int S, int K, uint8_t
 // in fp32 in slot order (y rows were already multiplied by topk_w).
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ ids,
                                                       int T, int H, int k, int E, uint16_t* __restrict__ out) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int h8n = H >> 3;
     const long long n = static_cast<long long>(T) * h8n;
     for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
@@ -170,9 +175,10 @@ cudaError_t launch_combine(const uint16_t* y, const int32_t* ids, int T, int H, 
     long long blocks = (n + 255) / 256;
     const long long cap = static_cast<long long>(sm_count()) * 8;
     if (blocks > cap) blocks = cap;
-    combine_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(y, ids, T, H, k, E, out);
+    const cudaError_t e = launch_chained(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, y, ids,
+                                         T, H, k, E, out);
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace kt

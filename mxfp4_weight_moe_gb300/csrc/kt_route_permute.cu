@@ -34,6 +34,8 @@ template <int EPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                          int renormalize, int32_t* __restrict__ ids,
                                                          float* __restrict__ w) {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ float s_v[kRouteTokensPerBlock][32];     // selected logits, in selection order
     __shared__ double s_ex[kRouteTokensPerBlock][32];   // their exp(l_j - l_max)
     __shared__ double s_part[kRouteTokensPerBlock];     // per-token sum
@@ -129,20 +131,26 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int reno
     if (T <= 0) return cudaSuccess;
     const int blocks = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
     const int epl = (E + 31) / 32;   // E <= kMaxExperts = 1024 keeps this <= 32
-    if (epl <= 1) route_topk_kernel<1><<<blocks, 256, 0, s>>>(logits, T, E, k, renormalize, ids, w);
-    else if (epl <= 2) route_topk_kernel<2><<<blocks, 256, 0, s>>>(logits, T, E, k, renormalize, ids, w);
-    else if (epl <= 4) route_topk_kernel<4><<<blocks, 256, 0, s>>>(logits, T, E, k, renormalize, ids, w);
-    else if (epl <= 8) route_topk_kernel<8><<<blocks, 256, 0, s>>>(logits, T, E, k, renormalize, ids, w);
-    else if (epl <= 16) route_topk_kernel<16><<<blocks, 256, 0, s>>>(logits, T, E, k, renormalize, ids, w);
-    else route_topk_kernel<32><<<blocks, 256, 0, s>>>(logits, T, E, k, renormalize, ids, w);
+    auto go = [&](auto kernel) {
+        return launch_chained(kernel, dim3(blocks), dim3(256), 0, s, logits, T, E, k, renormalize, ids, w);
+    };
+    cudaError_t e;
+    if (epl <= 1) e = go(route_topk_kernel<1>);
+    else if (epl <= 2) e = go(route_topk_kernel<2>);
+    else if (epl <= 4) e = go(route_topk_kernel<4>);
+    else if (epl <= 8) e = go(route_topk_kernel<8>);
+    else if (epl <= 16) e = go(route_topk_kernel<16>);
+    else e = go(route_topk_kernel<32>);
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ permute
 // Pass 1: per-tile expert histogram (tile = kPermTile consecutive slots).
 __global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restrict__ ids, long long S, int E,
                                                         int32_t* __restrict__ hist, int* err) {
+    griddep_wait();
+    griddep_launch_dependents();
     extern __shared__ int sh_count[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) sh_count[e] = 0;
     __syncthreads();
@@ -197,6 +205,8 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ h
                                                          int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ chunk_prefix,
                                                          int32_t* __restrict__ perm) {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ int s_warp[33];
     const int e = threadIdx.x;
     int run = 0;
@@ -240,6 +250,8 @@ __global__ void __launch_bounds__(128) perm_scatter_kernel(const int32_t* __rest
                                                            const int32_t* __restrict__ offsets,
                                                            int32_t* __restrict__ perm,
                                                            int32_t* __restrict__ inv_perm) {
+    griddep_wait();
+    griddep_launch_dependents();
     extern __shared__ int sh[];
     int* s_base = sh;                      // [E]   offsets[e] + tile prefix, then running count
     int* s_id = sh + E;                    // [kPermTile] expert of each slot (-1 invalid / past S)
@@ -302,6 +314,8 @@ __global__ void __launch_bounds__(1024) perm_fused_kernel(const int32_t* __restr
                                                           int32_t* __restrict__ chunk_prefix,
                                                           int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm,
                                                           int* err) {
+    griddep_wait();
+    griddep_launch_dependents();
     extern __shared__ int s_cnt[];   // [32][E]: counts, then bases
     __shared__ int s_warp[33];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -397,27 +411,30 @@ cudaError_t launch_permute(const int32_t* ids, long long S, int E, int32_t* hist
             attr_set[dev] = true;
         }
         if (S > 0) {
-            perm_fused_kernel<<<1, 1024, 32 * E * sizeof(int), s>>>(ids, static_cast<int>(S), E, expert_offsets,
-                                                                   chunk_prefix, perm, inv_perm, err);
+            const cudaError_t e = launch_chained(perm_fused_kernel, dim3(1), dim3(1024), 32 * E * sizeof(int), s, ids,
+                                                 static_cast<int>(S), E, expert_offsets, chunk_prefix, perm,
+                                                 inv_perm, err);
             count_launches(1);
-            return cudaGetLastError();
+            return e != cudaSuccess ? e : cudaGetLastError();
         }
     }
     if (ntiles > 0) {
-        perm_hist_kernel<<<ntiles, 256, E * sizeof(int), s>>>(ids, S, E, hist, err);
+        cudaError_t e = launch_chained(perm_hist_kernel, dim3(ntiles), dim3(256), E * sizeof(int), s, ids, S, E, hist,
+                                       err);
         count_launches(1);
-        cudaError_t e = cudaGetLastError();
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    perm_scan_kernel<<<1, 1024, 0, s>>>(hist, ntiles, E, S, expert_offsets, chunk_prefix, perm);
+    cudaError_t e = launch_chained(perm_scan_kernel, dim3(1), dim3(1024), 0, s, hist, ntiles, E, S, expert_offsets,
+                                   chunk_prefix, perm);
     count_launches(1);
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (ntiles > 0) {
-        perm_scatter_kernel<<<ntiles, 128, (E + 2 * kPermTile) * sizeof(int), s>>>(ids, S, E, hist, expert_offsets,
-                                                                                     perm, inv_perm);
+        e = launch_chained(perm_scatter_kernel, dim3(ntiles), dim3(128), (E + 2 * kPermTile) * sizeof(int), s, ids, S,
+                           E, hist, expert_offsets, perm, inv_perm);
         count_launches(1);
-        e = cudaGetLastError();
+        if (e == cudaSuccess) e = cudaGetLastError();
     }
     return e;
 }
