@@ -53,7 +53,7 @@ FP8_OVER_BF16 = 2.0     # nominal dense ratio (4.5 / 2.25 PFLOP/s); mxf8f6f4 run
 # figure no longer applies and the bench line reports traffic null.
 GEMM_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mxfp4_weight_moe_gb300", "csrc", "kt_gemm_mx.cu")
 FC1_TRAFFIC = {
-    ("dsv4", "6503a929a318ea51de4dc290a3e2d15dba2f2f1e9bf139d7faa034d921d4a0ac"): 2767272192 + 47961088,
+    ("dsv4", "7256a02b1aee55be92098b21f6082b330943513e44007f0d6e5573f12578dc53"): 2753858560 + 47398912,
 }
 
 
