@@ -53,7 +53,7 @@ FP8_OVER_BF16 = 2.0     # nominal dense ratio (4.5 / 2.25 PFLOP/s); mxf8f6f4 run
 # figure no longer applies and the bench line reports traffic null.
 GEMM_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mxfp4_weight_moe_gb300", "csrc", "kt_gemm_mx.cu")
 FC1_TRAFFIC = {
-    ("dsv4", "7256a02b1aee55be92098b21f6082b330943513e44007f0d6e5573f12578dc53"): 2753858560 + 47398912,
+    ("dsv4", "d24202785e1bedaa3b238f9315d0a8d921266b5d928636db0d1eb5247ac0ed09"): 2747439360 + 47791360,
 }
 
 

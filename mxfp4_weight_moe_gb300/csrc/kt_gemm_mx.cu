@@ -826,14 +826,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<__nv_bfloat16*>(tb + j * 80 + lane * 2) = b;
                     }
                     __syncwarp();
-                    if (mine) {
-                        const uint4* src = reinterpret_cast<const uint4*>(tb + lane * 80);
-                        uint4* dst =
-                            reinterpret_cast<uint4*>(p.y + static_cast<size_t>(slot) * p.H + ti.f * 128 + q * 32);
-                        dst[0] = src[0];
-                        dst[1] = src[1];
-                        dst[2] = src[2];
-                        dst[3] = src[3];
+                    // four lanes per token row: each store instruction writes 8 rows x 64
+                    // contiguous bytes (full sectors; one lane per row left each 32-byte
+                    // sector half-written per instruction)
+                    const int mine_i = mine ? 1 : 0;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int tk = r * 8 + (lane >> 2);
+                        const int sl = __shfl_sync(0xffffffffu, slot, tk);
+                        const int mk = __shfl_sync(0xffffffffu, mine_i, tk);
+                        if (mk) {
+                            const uint4 val = *reinterpret_cast<const uint4*>(tb + tk * 80 + (lane & 3) * 16);
+                            uint4* dst = reinterpret_cast<uint4*>(p.y + static_cast<size_t>(sl) * p.H + ti.f * 128 +
+                                                                  q * 32) +
+                                         (lane & 3);
+                            *dst = val;
+                        }
                     }
                     __syncwarp();
                 } else {
