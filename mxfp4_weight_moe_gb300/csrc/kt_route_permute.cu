@@ -242,9 +242,15 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ h
 
 // Pass 3 (one block of 128 threads per tile): the tile's ids and the
 // per-expert bases (expert offset + tile prefix) are staged in shared memory
-// first; then one warp sweeps the tile in slot order, 32 slots per round,
-// finding the peers of each slot with match.any so that equal experts keep
-// their slot order.  Ranks and outputs are written back by all 128 threads.
+// first.  Warp w owns the tile's slots [256 w, 256 w + 256): it counts them
+// per expert (match.any, one lane per distinct expert adding the round's
+// count), an exclusive prefix over the four warps turns the counts into
+// per-warp bases, and each warp then sweeps its slots in slot order, ranking
+// peers with match.any, so equal experts keep slot order across rounds and
+// warps.  Ranks and outputs are written back by all 128 threads.
+constexpr int kScatterWarps = 4;
+constexpr int kScatterSeg = kPermTile / kScatterWarps;
+
 __global__ void __launch_bounds__(128) perm_scatter_kernel(const int32_t* __restrict__ ids, long long S, int E,
                                                            const int32_t* __restrict__ tile_base,
                                                            const int32_t* __restrict__ offsets,
@@ -253,12 +259,14 @@ __global__ void __launch_bounds__(128) perm_scatter_kernel(const int32_t* __rest
     griddep_wait();
     griddep_launch_dependents();
     extern __shared__ int sh[];
-    int* s_base = sh;                      // [E]   offsets[e] + tile prefix, then running count
+    int* s_base = sh;                      // [E]   offsets[e] + tile prefix
     int* s_id = sh + E;                    // [kPermTile] expert of each slot (-1 invalid / past S)
     int* s_pos = s_id + kPermTile;         // [kPermTile] permuted row of each slot
+    int* s_w = s_pos + kPermTile;          // [kScatterWarps][E] per-warp counts, then running bases
     const long long base = static_cast<long long>(blockIdx.x) * kPermTile;
     const int32_t* tb = tile_base + static_cast<size_t>(blockIdx.x) * E;
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_base[e] = offsets[e] + tb[e];
+    for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) s_w[i] = 0;
     for (int i = threadIdx.x; i < kPermTile; i += blockDim.x) {
         const long long s = base + i;
         int e = -1;
@@ -269,20 +277,34 @@ __global__ void __launch_bounds__(128) perm_scatter_kernel(const int32_t* __rest
         s_id[i] = e;
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        for (int r = 0; r < kPermTile / 32; ++r) {
-            if (base + r * 32 >= S) break;   // warp-uniform
-            const int e = s_id[r * 32 + lane];
-            const unsigned peers = __match_any_sync(0xffffffffu, e);
-            const int rank = __popc(peers & ((1u << lane) - 1u));
-            const int leader = __ffs(peers) - 1;
-            const int before = (e >= 0) ? s_base[e] : 0;
-            __syncwarp();
-            if (e >= 0 && lane == leader) s_base[e] = before + __popc(peers);
-            __syncwarp();
-            s_pos[r * 32 + lane] = (e >= 0) ? before + rank : -1;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int* cnt = s_w + warp * E;
+    const int i0 = warp * kScatterSeg;
+    for (int r = 0; r < kScatterSeg / 32; ++r) {
+        const int e = s_id[i0 + r * 32 + lane];
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) cnt[e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = s_base[e];
+        for (int w = 0; w < kScatterWarps; ++w) {
+            const int c = s_w[w * E + e];
+            s_w[w * E + e] = run;
+            run += c;
         }
+    }
+    __syncthreads();
+    for (int r = 0; r < kScatterSeg / 32; ++r) {
+        const int e = s_id[i0 + r * 32 + lane];
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        const int before = (e >= 0) ? cnt[e] : 0;
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) cnt[e] = before + __popc(peers);
+        __syncwarp();
+        s_pos[i0 + r * 32 + lane] = (e >= 0) ? before + rank : -1;
     }
     __syncthreads();
     for (int i = threadIdx.x; i < kPermTile; i += blockDim.x) {
@@ -431,8 +453,9 @@ cudaError_t launch_permute(const int32_t* ids, long long S, int E, int32_t* hist
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (ntiles > 0) {
-        e = launch_chained(perm_scatter_kernel, dim3(ntiles), dim3(128), (E + 2 * kPermTile) * sizeof(int), s, ids, S,
-                           E, hist, expert_offsets, perm, inv_perm);
+        e = launch_chained(perm_scatter_kernel, dim3(ntiles), dim3(128),
+                           ((1 + kScatterWarps) * E + 2 * kPermTile) * sizeof(int), s, ids, S, E, hist,
+                           expert_offsets, perm, inv_perm);
         count_launches(1);
         if (e == cudaSuccess) e = cudaGetLastError();
     }
