@@ -43,6 +43,12 @@
  *   - A workspace may be reused by consecutive calls on one stream; calls
  *     that share a workspace must not overlap on the GPU.
  *   - Kernels are built for sm_103a only; other devices get KT_ERR_CUDA.
+ *   - Every kernel is launched with programmatic stream serialization (it
+ *     may be scheduled while the previous work in the stream finishes) and
+ *     waits for that work to complete before it touches memory, so stream
+ *     order is kept; each also lets the next launch in the stream start
+ *     early, which matters only to a caller kernel that opts in to the
+ *     same mechanism, and which must then wait before reading our outputs.
  */
 #ifndef KT_MOE_H
 #define KT_MOE_H
