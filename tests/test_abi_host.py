@@ -195,3 +195,45 @@ def test_debug_configure_rejects_unknown_flags():
 def test_profile_stage_mask_rejects_unknown_stages():
     assert kt.lib().kt_moe_profile_enable_stages(1 << len(kt.STAGES)) == -1   # KT_ERR_INVALID_ARG
     assert kt.lib().kt_moe_profile_enable_stages(0) == 0
+
+
+def _kernel_bodies(src: str) -> dict:
+    """name -> body text of every __global__ function in a CUDA source."""
+    import re
+    out = {}
+    for m in re.finditer(r"__global__\s+void\s+(?:__launch_bounds__\([^)]*\)\s*)?(\w+)\s*\(", src):
+        start = src.index("{", m.end())
+        depth, i = 0, start
+        while True:
+            if src[i] == "{":
+                depth += 1
+            elif src[i] == "}":
+                depth -= 1
+                if depth == 0:
+                    break
+            i += 1
+        out[m.group(1)] = src[start:i + 1]
+    return out
+
+
+def test_chained_kernels_wait_before_touching_memory():
+    """Kernels launched with programmatic stream serialization may start while
+    their predecessor runs; each must call griddep_wait() before its first
+    global-memory access (checked here as: before any pointer argument is
+    read through __ldg, an index or a dereference of a kernel parameter)."""
+    import glob
+    import os
+    import re
+    csrc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "mxfp4_weight_moe_gb300", "csrc")
+    src = "\n".join(open(f).read() for f in sorted(glob.glob(os.path.join(csrc, "*.cu"))))
+    # launch_chained(<kernel>, ...) calls, and the routing launcher's go(route_topk_kernel<EPL>)
+    chained = (set(re.findall(r"launch_chained\((\w+)", src)) - {"kernel"}) | set(re.findall(r"go\((\w+)<", src))
+    assert "cudaLaunchAttributeProgrammaticStreamSerialization" in src
+    chained.add("mx_gemm_kernel")   # launched with the attribute through cudaLaunchKernelEx
+    bodies = _kernel_bodies(src)
+    assert chained <= set(bodies), chained - set(bodies)
+    for name in sorted(chained):
+        body = bodies[name]
+        assert "griddep_wait();" in body, name
+        before = body[:body.index("griddep_wait();")]
+        assert "__ldg(" not in before and not re.search(r"\bp\.\w+\s*\[", before), name
