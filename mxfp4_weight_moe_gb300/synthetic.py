@@ -64,6 +64,11 @@ CONFIGS: dict[str, MoEConfig] = {
     # Kimi-K3-shaped layer (SwiGLU in place of SiTU), uniform router logits
     "kimi_T16": MoEConfig("kimi_T16", T=16, H=7168, E=896, k=16, I=3584, logits="uniform"),
     "kimi_T8192": MoEConfig("kimi_T8192", T=8192, H=7168, E=896, k=16, I=3584, logits="uniform"),
+    # profiling-sized Kimi-K3-shaped layers: 64 of the 896 experts, so that a
+    # multi-pass ncu capture holds a few GB on the device; tiles as in
+    # kimi_T16 (16 token rows) and kimi_T8192 (about 176 rows per chunk)
+    "kimi_T16_e64": MoEConfig("kimi_T16_e64", T=16, H=7168, E=64, k=16, I=3584, logits="uniform"),
+    "kimi_T2048_e64": MoEConfig("kimi_T2048_e64", T=2048, H=7168, E=64, k=16, I=3584, logits="uniform"),
     # layerwise prefill: 43 DSV4-shaped layers, layer l's logits use seed l
     "layerwise": MoEConfig("layerwise", T=16384, H=4096, E=256, k=6, I=2048, logits="zipf", layers=43),
 }
