@@ -1,5 +1,5 @@
 #!/usr/bin/env python
-"""Benchmark of the fused MXFP4-weight MoE layer on GB300: tokens/s and the
+"""Benchmark of the fused MXFP4-weight MoE layer on one GB300: tokens/s and the
 fraction of the block-scaled roofline.
 
 One step = one pass of the layer's hot path over one batch: top-k routing
@@ -10,16 +10,22 @@ when the timed region starts; ``e2e`` repeats the measurement with the
 step's inputs (hidden, logits) copied from pinned host memory and the output
 copied back inside the timed region.
 
-Default workload: the DeepSeek-V4-Flash-shaped layer (T=4096 tokens, H=4096,
-E=256 experts, top-6, I=2048, Zipf(1.1)-skewed router logits).  Its expert
-weights (3.3 GB) are far larger than L2, so every step streams them from HBM
-(no L2 flush is needed between steps).
+Default workload: the Kimi-K3-shaped layer at T=8192 prefill tokens (H=7168,
+E=896 experts, top-16, I=3584, uniform router logits; 36.7 GB of packed
+experts, all resident), the largest configuration that fits one GPU.  The
+DeepSeek-V4-Flash-shaped layer (T=4096, H=4096, E=256, top-6, I=2048,
+Zipf(1.1) skew) is measured after it and nested under "secondary".  Expert
+weights far exceed L2, so every step streams them from HBM (no L2 flush is
+needed between steps).
 
 ``--impl reference`` times the fp64 CPU oracle (the only reference
 implementation; the pages ship no code) on the host cores, on a bounded
 token sample per step, and prints the same JSON line with "impl":
-"reference".  Under torchrun (N > 1) every rank runs an independent replica
-(the layer does not shard on one GPU per box); rank 0 prints the line.
+"reference".
+
+The layer runs on one GPU: it is not sharded and has no collective step.
+Multi-GPU runs (``--gpus N`` with N > 1, or WORLD_SIZE > 1 under torchrun)
+print an "unavailable" line on rank 0 and exit without touching a GPU.
 """
 from __future__ import annotations
 
@@ -47,10 +53,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FP8_OVER_BF16 = 2.0     # nominal dense ratio (4.5 / 2.25 PFLOP/s); mxf8f6f4 runs at the fp8 rate
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one FC1 launch
-# from an ncu capture of `python bench.py --warmup 3 --steps 1
-# --no-cpu-baseline` (profiles/mx_gemm_dsv4.md), keyed by workload and by the
-# SHA-256 of the GEMM source it was taken on: once the kernel changes, the
-# figure no longer applies and the bench line reports traffic null.
+# from an ncu capture (the summaries under profiles/ give the command), keyed
+# by workload and by the SHA-256 of the GEMM source it was taken on: once the
+# kernel changes, the figure no longer applies and the bench line reports
+# traffic null.
 GEMM_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mxfp4_weight_moe_gb300", "csrc", "kt_gemm_mx.cu")
 FC1_TRAFFIC = {
     ("dsv4", "d24202785e1bedaa3b238f9315d0a8d921266b5d928636db0d1eb5247ac0ed09"): 2747439360 + 47791360,
@@ -74,38 +80,6 @@ def load_peaks():
             d = json.load(f)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
-
-
-# ------------------------------------------------------------------ distributed
-def dist_setup(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-
-        backend = "nccl" if args.impl == "ours" else "gloo"
-        if backend == "nccl":
-            torch.cuda.set_device(local)
-        dist.init_process_group(backend=backend)
-    return world, rank, local
-
-
-def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.barrier()
-
-
-def max_over_ranks(x: float, world: int, device) -> float:
-    if world == 1:
-        return x
-    import torch.distributed as dist
-
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
 
 
 # ------------------------------------------------------------------ clocks
@@ -200,83 +174,129 @@ def workload_desc(cfg):
             f"logits={cfg.logits} seed={cfg.seed}")
 
 
-# ------------------------------------------------------------------ CPU oracle
-def oracle_tokens_per_s(cfg, hidden, ids_np, w_np, W_host, n_tokens, seed=0):
+# ------------------------------------------------------------------ CPU oracle on token samples
+def config_block(cfg, touched: int, work: dict) -> dict:
+    """The line's "config" (identical for this arm and the reference arm)."""
+    return {"workload": workload_desc(cfg), "T": cfg.T, "H": cfg.H, "E": cfg.E, "top_k": cfg.k, "I": cfg.I,
+            "touched_experts": touched, "parallelism": "single",
+            "l2": f"inputs larger than L2 ({work['layer_bytes'] / 1e9:.2f} GB of weights+activations per step)"}
+
+
+class ExpertSource:
+    """Packed weights of chosen experts, as host arrays for the oracle.
+
+    Either slices of device-resident weight tensors, or each expert
+    regenerated by the seeded input generator (every expert has its own
+    generator, so a subset comes out byte-identical to the full tensors made
+    on the same kind of device).  Only the experts a token sample touches
+    are ever copied to the host: the Kimi-K3-shaped layer holds 36.7 GB."""
+
+    def __init__(self, cfg, W=None, device="cpu"):
+        self.cfg, self.W, self.device = cfg, W, device
+
+    def fetch(self, experts: np.ndarray):
+        if self.W is not None:
+            idx = torch.from_numpy(experts.astype(np.int64)).to(self.W[0].device)
+            return [t.index_select(0, idx).cpu().numpy() for t in self.W]
+        parts = [syn.make_expert(int(e), self.cfg.H, self.cfg.I, self.cfg.seed, self.device) for e in experts]
+        out = [torch.stack([p[i] for p in parts]).cpu().numpy() for i in range(4)]
+        del parts
+        return out
+
+
+def oracle_batch(hb, ids, w, src: ExpertSource, tokens: np.ndarray, E: int) -> float:
+    """The oracle forward for `tokens` (routing given), using only the experts
+    they touch (ids remapped to that compact list).  Returns the seconds the
+    oracle call took (the weight fetch is not counted)."""
     import oracle as O
 
-    rng = np.random.default_rng(seed)
-    toks = np.sort(rng.choice(cfg.T, size=min(n_tokens, cfg.T), replace=False)).astype(np.int32)
-    hb = hidden.cpu().view(torch.int16).numpy().view(np.uint16)
+    sub = ids[tokens]
+    ok = (sub >= 0) & (sub < E)
+    used = np.unique(sub[ok])
+    remap = np.full(E, -1, np.int64)
+    remap[used] = np.arange(used.shape[0])
+    rid = np.where(ok, remap[np.clip(sub, 0, E - 1)], -1).astype(np.int32)
+    Wh = src.fetch(used)
     t0 = time.perf_counter()
-    O.moe_forward(hb, ids_np, w_np, *W_host, tokens=toks, want=("out",))
-    dt = time.perf_counter() - t0
-    return len(toks) / dt, dt, len(toks)
+    O.moe_forward(np.ascontiguousarray(hb[tokens]), rid, np.ascontiguousarray(w[tokens]), *Wh, want=("out",))
+    return time.perf_counter() - t0
 
 
-def cpu_baseline(cfg, hidden, logits, W, target_s=12.0):
+def cpu_baseline(cfg, hidden, ids_np, w_np, W, target_s=12.0):
+    """The fp64 oracle on the host cores, on seeded batches of tokens until
+    about target_s seconds of oracle time have run (routing excluded)."""
     import oracle as O
 
-    W_host = [t.cpu().numpy() for t in W]
-    lg = logits.cpu().numpy()
-    ids_np, w_np = O.route(lg, cfg.k)
-    rate, dt, n = oracle_tokens_per_s(cfg, hidden, ids_np, w_np, W_host, 16)
-    n2 = int(min(cfg.T, max(16, rate * target_s)))
-    rate, dt, n = oracle_tokens_per_s(cfg, hidden, ids_np, w_np, W_host, n2, seed=1)
-    return {"value": rate, "unit": "tokens/s", "cores": O.max_threads(), "kind": "oracle",
-            "sample": f"{n} of {cfg.T} tokens (seeded, all {cfg.k} experts each) through the fp64 oracle "
-                      f"forward ({dt:.1f} s); routing excluded"}
+    threads = O.max_threads()
+    batch = max(1, threads)
+    hb = hidden.cpu().view(torch.int16).numpy().view(np.uint16)
+    order = np.random.default_rng(1).permutation(cfg.T).astype(np.int32)
+    src = ExpertSource(cfg, W=W)
+    spent, done = 0.0, 0
+    while done < cfg.T and (spent < target_s or done == 0):
+        toks = np.sort(order[done:done + batch])
+        spent += oracle_batch(hb, ids_np, w_np, src, toks, cfg.E)
+        done += toks.shape[0]
+    return {"value": done / spent, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{done} of {cfg.T} tokens (seeded, in batches of {batch}, all {cfg.k} experts each) "
+                      f"through the fp64 oracle forward ({spent:.1f} s of oracle time); routing excluded"}
 
 
 # ------------------------------------------------------------------ arms
-def run_reference(args, cfg, world, rank):
-    if rank != 0:
-        return None
+def run_reference(args, cfg):
+    """The fp64 oracle as the reference arm: every step routes and runs the
+    layer forward on a seeded token sample on the host cores."""
     import oracle as O
 
-    dev = "cpu"
-    hidden = syn.make_hidden(cfg.T, cfg.H, cfg.seed, device=dev)
-    logits = syn.make_logits(cfg.T, cfg.E, cfg.logits, cfg.seed, device=dev)
-    W = syn.make_weights(cfg.E, cfg.H, cfg.I, seed=cfg.seed, device=dev)
-    W_host = [t.numpy() for t in W]
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"   # the seeded input generator only
+    hidden = syn.make_hidden(cfg.T, cfg.H, cfg.seed, device=gen_dev).cpu()
+    logits = syn.make_logits(cfg.T, cfg.E, cfg.logits, cfg.seed, device=gen_dev).cpu()
     hb = hidden.view(torch.int16).numpy().view(np.uint16)
     lg = logits.numpy()
-    # calibrate tokens per step so the whole run takes about `budget` seconds
-    budget = float(args.ref_budget_s)
-    t0 = time.perf_counter()
-    ids, w = O.route(lg[:8], cfg.k)
-    O.moe_forward(hb[:8], ids, w, *W_host, want=("out",))
-    per_tok = (time.perf_counter() - t0) / 8
-    n_per_step = int(max(1, min(cfg.T, budget / max(1, args.steps + args.warmup) / per_tok)))
+    ids_all, _ = O.route(lg, cfg.k)
+    touched = int((np.bincount(ids_all.reshape(-1), minlength=cfg.E) > 0).sum())
+    work = algorithmic(cfg, touched)
+    full_bytes = cfg.E * (work["w13_bytes_per_expert"] + work["w2_bytes_per_expert"])
+    if full_bytes <= 8e9:   # small enough to hold every expert on the host once
+        W = syn.make_weights(cfg.E, cfg.H, cfg.I, seed=cfg.seed, device=gen_dev)
+        src = ExpertSource(cfg, W=W)
+    else:                   # regenerate only the experts each step's tokens touch
+        src = ExpertSource(cfg, device=gen_dev)
+    threads = O.max_threads()
     rng = np.random.default_rng(0)
 
-    def step(i):
-        toks = np.sort(rng.choice(cfg.T, size=n_per_step, replace=False))
+    def step(n):
+        toks = np.sort(rng.choice(cfg.T, size=n, replace=False)).astype(np.int32)
+        t0 = time.perf_counter()
         ids, w = O.route(lg[toks], cfg.k)
-        O.moe_forward(hb[toks], ids, w, *W_host, want=("out",))
+        t_route = time.perf_counter() - t0
+        return t_route + oracle_batch(hb[toks], ids, w, src, np.arange(n, dtype=np.int32), cfg.E)
 
-    for i in range(args.warmup):
-        step(i)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        step(i)
-    dt = time.perf_counter() - t0
+    # size each step so that the whole run takes about ref_budget_s of oracle time
+    per_step = float(args.ref_budget_s) / max(1, args.steps + args.warmup)
+    t_cal = step(max(1, threads))
+    n_per_step = int(max(1, min(cfg.T, threads * per_step / max(t_cal, 1e-6))))
+    for _ in range(args.warmup):
+        step(n_per_step)
+    dt = sum(step(n_per_step) for _ in range(args.steps))
     value = n_per_step * args.steps / dt
-    sample = (f"{n_per_step} of {cfg.T} tokens per step (seeded), route + forward in fp64 on the host cores; "
-              f"{args.steps} steps in {dt:.1f} s")
+    sample = (f"{n_per_step} of {cfg.T} tokens per step (seeded), route + forward in fp64 on the host cores "
+              f"({threads} threads); {args.steps} steps, {dt:.1f} s of oracle time (input generation and weight "
+              f"fetch excluded)")
     return {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(cfg), "T": cfg.T, "H": cfg.H, "E": cfg.E, "top_k": cfg.k,
-                   "I": cfg.I, "parallelism": "replicas", "l2": "n/a (host)"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": O.max_threads(), "kind": "oracle",
-                         "sample": sample},
+        "config": config_block(cfg, touched, work),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
-def run_ours(args, cfg, world, rank, local):
-    dev = torch.device("cuda", local)
+def run_ours(args, cfg, full: bool = True):
+    """Device-resident timing, e2e with host copies, CUDA-graph replay, the
+    roofline of the dominant kernel and (full=True) the CPU baseline."""
+    dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
     hidden = syn.make_hidden(cfg.T, cfg.H, cfg.seed, device=dev)
@@ -305,7 +325,6 @@ def run_ours(args, cfg, world, rank, local):
     # ---- timed region: device-resident inputs
     sampler = ClockSampler(dev)
     sampler.start()
-    barrier(world)
     torch.cuda.synchronize(dev)
     launches0 = kt.kernel_launches()
     # inside the timed region only the roofline kernel (FC1) is bracketed by
@@ -317,7 +336,6 @@ def run_ours(args, cfg, world, rank, local):
         step()
     ev1.record(stream)
     torch.cuda.synchronize(dev)
-    barrier(world)
     elapsed_ms = ev0.elapsed_time(ev1)
     launches = kt.kernel_launches() - launches0
     prof_fc1 = kt.profile_read()["fc1"]
@@ -330,8 +348,8 @@ def run_ours(args, cfg, world, rank, local):
         step()
     prof = kt.profile_read()
     kt.profile_enable(False)
-    ms_per_step = max_over_ranks(elapsed_ms / args.steps, world, dev)
-    value = T * world / (ms_per_step / 1e3)
+    ms_per_step = elapsed_ms / args.steps
+    value = T / (ms_per_step / 1e3)
 
     # ---- e2e: host buffers in, host buffer out, copies inside the timed region.  As a serving
     # loop would run it: inputs and outputs double-buffered, host->device copies on one stream
@@ -382,7 +400,6 @@ def run_ours(args, cfg, world, rank, local):
     for i in range(4):
         e2e_step(i)
     torch.cuda.synchronize(dev)
-    barrier(world)
     ev0.record(stream)
     s_in.wait_stream(stream)                   # the first copy starts inside the timed region
     for i in range(e2e_steps):
@@ -390,7 +407,7 @@ def run_ours(args, cfg, world, rank, local):
     stream.wait_stream(s_out)                  # ... and the last result is on the host before it ends
     ev1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e2e_steps, world, dev)
+    e2e_ms = ev0.elapsed_time(ev1) / e2e_steps
     last = (e2e_steps - 1) % 2
     assert torch.equal(out_host[last].view(torch.int16), out.cpu().view(torch.int16))
 
@@ -412,8 +429,8 @@ def run_ours(args, cfg, world, rank, local):
             g.replay()
         ev1.record(stream)
         torch.cuda.synchronize(dev)
-        g_ms = max_over_ranks(ev0.elapsed_time(ev1) / reps, world, dev)
-        graph = {"value": T * world / (g_ms / 1e3), "unit": "tokens/s", "ms_per_step": g_ms, "replays": reps}
+        g_ms = ev0.elapsed_time(ev1) / reps
+        graph = {"value": T / (g_ms / 1e3), "unit": "tokens/s", "ms_per_step": g_ms, "replays": reps}
         del g
     except Exception as exc:  # noqa: BLE001 - reported, never fatal to the bench line
         graph = {"error": f"{type(exc).__name__}: {exc}"[:200]}
@@ -427,13 +444,11 @@ def run_ours(args, cfg, world, rank, local):
     fc1_gbs = work["fc1_bytes"] / (fc1_ms / 1e3) / 1e9
     t_roof_ms = 1e3 * max(work["layer_flops"] / (mx_tflops * 1e12), work["layer_bytes"] / (hbm * 1e9))
     res = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxfp8xmxfp4", "data": "synthetic",
-        "config": {"workload": workload_desc(cfg), "T": T, "H": H, "E": E, "top_k": k, "I": I,
-                   "touched_experts": touched, "parallelism": "replicas" if world > 1 else "single",
-                   "l2": f"inputs larger than L2 ({work['layer_bytes'] / 1e9:.2f} GB of weights+activations per step)"},
-        "e2e": {"value": T * world / (e2e_ms / 1e3), "unit": "tokens/s",
+        "config": config_block(cfg, touched, work),
+        "e2e": {"value": T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "copies": "overlapped (separate H2D and D2H streams, double-buffered)" if overlap else "in order",
                 "h2d_bytes_per_step": hidden.numel() * 2 + logits.numel() * 4,
                 "d2h_bytes_per_step": out.numel() * 2},
@@ -453,18 +468,45 @@ def run_ours(args, cfg, world, rank, local):
                          "the roofline's FC1 time is measured inside it",
         "fc2_gbs": work["fc2_bytes"] / (fc2_ms / 1e3) / 1e9 if fc2_ms > 0 else None,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(cfg, hidden, logits, W)
+    if full and not args.no_cpu_baseline:
+        ids_np = route_out[0].cpu().numpy()
+        w_np = route_out[1].cpu().numpy()
+        res["cpu_baseline"] = cpu_baseline(cfg, hidden, ids_np, w_np, W)
+    del W
+    torch.cuda.empty_cache()
     return res
 
 
-def run_layerwise(args, cfg, world, rank, local):
+def secondary_summary(res: dict) -> dict:
+    keep = ("value", "unit", "ms_per_step", "config", "e2e", "gpu_launches", "graph", "roofline", "layer_roofline",
+            "stage_ms", "fc2_gbs", "clocks")
+    return {k: res[k] for k in keep if k in res}
+
+
+def _h2d_best(pack, dst, stream, reps: int) -> float:
+    """Best pinned host -> device copy rate (GB/s) of one pack over `reps` copies."""
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = 0.0
+    for _ in range(reps):
+        ev0.record(stream)
+        dst.copy_(pack, non_blocking=True)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        best = max(best, pack.numel() / (ev0.elapsed_time(ev1) / 1e3) / 1e9)
+    return best
+
+
+def run_layerwise(args, cfg):
     """Layerwise prefill over cfg.layers DSV4-shaped layers at T tokens.
 
     Expert weights live in pinned host memory: P distinct layer stores used
     cyclically (layer l streams store l mod P), so the host link moves one
-    full 3.42 GB pack per layer while the pinned footprint stays P packs."""
-    dev = torch.device("cuda", local)
+    full 3.42 GB pack per layer while the pinned footprint stays P packs.
+    The link's rate is the best of several pack copies taken before and after
+    the timed prefills; the library's per-layer events give each layer's copy
+    and compute busy times; the serialized control (upload -> compute ->
+    synchronise per layer) is timed over the same number of steps."""
+    dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     L, T, H, E, k, I = cfg.layers, cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
     P = max(1, min(args.layer_stores, L))
@@ -476,60 +518,70 @@ def run_layerwise(args, cfg, world, rank, local):
     pack_bytes = kt.Layerwise.pack_bytes(H, I, E)
     hidden = syn.make_hidden(T, H, cfg.seed, device=dev)
     logits = [syn.make_logits(T, E, cfg.logits, seed=l, device=dev) for l in range(L)]
-    lw = kt.Layerwise([packs[l % P] for l in range(L)], H, I, E, k, T_max=T)
+    lw = kt.Layerwise([packs[l % P] for l in range(L)], H, I, E, k, T_max=T, zero_copy=args.zero_copy)
     out = torch.empty_like(hidden)
     stream = torch.cuda.current_stream(dev)
-    # pinned host -> device copy bandwidth of one pack (the link this mode is bound by)
     probe_dst = torch.empty(pack_bytes, dtype=torch.uint8, device=dev)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    probe_dst.copy_(packs[0], non_blocking=True)
-    ev0.record(stream)
-    for _ in range(3):
-        probe_dst.copy_(packs[0], non_blocking=True)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    h2d_gbs = 3 * pack_bytes / (ev0.elapsed_time(ev1) / 1e3) / 1e9
-    del probe_dst
+    link_before = max(_h2d_best(p, probe_dst, stream, 2) for p in packs)
     for _ in range(args.warmup):
         lw.prefill(hidden, logits, out=out)
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev)
     sampler.start()
-    barrier(world)
     launches0 = kt.kernel_launches()
+    lw.enable_timing(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(args.steps):
         lw.prefill(hidden, logits, out=out)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
-    barrier(world)
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
+    ms = ev0.elapsed_time(ev1) / args.steps
     launches = kt.kernel_launches() - launches0
     clocks = sampler.stop()
-    # serialized control: upload all experts -> compute -> synchronise, per layer
-    t0 = time.perf_counter()
-    lw.prefill(hidden, logits, out=out, serialized=True)
+    per_layer = lw.timing()          # the last prefill's per-layer copy / compute busy times
+    lw.enable_timing(False)
+    link_after = max(_h2d_best(p, probe_dst, stream, 2) for p in packs)
+    del probe_dst
+    # serialized control over the same number of steps
     torch.cuda.synchronize(dev)
-    ms_serial = 1e3 * (time.perf_counter() - t0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        lw.prefill(hidden, logits, out=out, serialized=True)
+    torch.cuda.synchronize(dev)
+    ms_serial = 1e3 * (time.perf_counter() - t0) / args.steps
     lw.close()
+    h2d_gbs = max(link_before, link_after)
     link_gbs = L * pack_bytes / (ms / 1e3) / 1e9
     t_roof_ms = 1e3 * L * pack_bytes / (h2d_gbs * 1e9)
+    touched = E
+    work = algorithmic(cfg, touched)
+    cfgb = config_block(cfg, touched, work)
+    cfgb.update({"workload": f"layerwise: {L} layers x ({workload_desc(cfg)}), {P} distinct pinned host stores "
+                             f"cycled", "layers": L, "pinned_host_GB": P * pack_bytes / 1e9,
+                 "weights": "read in place from pinned host memory" if args.zero_copy else
+                            "streamed into two device slots, double-buffered",
+                 "l2": "inputs larger than L2 (3.42 GB streamed per layer)"})
+    copy_ms = [c for c, _ in per_layer["layers"]]
+    comp_ms = [m for _, m in per_layer["layers"]]
     return {
-        "metric": METRIC, "value": T * world / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "mxfp8xmxfp4", "data": "synthetic",
-        "config": {"workload": f"layerwise: {L} layers x ({workload_desc(cfg)}), {P} distinct pinned host stores "
-                               f"cycled", "T": T, "H": H, "E": E, "top_k": k, "I": I, "layers": L,
-                   "pinned_host_GB": P * pack_bytes / 1e9, "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (3.42 GB streamed per layer)"},
-        "e2e": {"value": T * world / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": L * pack_bytes,
+        "vs_baseline": None, "dtype": "mxfp8xmxfp4", "data": "synthetic", "config": cfgb,
+        "e2e": {"value": T / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": L * pack_bytes,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": int(launches), "clocks": clocks,
         "roofline": {"bound": "h2d", "achieved": link_gbs, "peak": h2d_gbs, "unit": "GB/s",
                      "frac": link_gbs / h2d_gbs, "traffic": None,
-                     "kernel": "host->device expert streaming (copy engine)",
-                     "peak_source": "pinned H2D copy of one pack, measured in this run"},
+                     "kernel": "host->device expert streaming" + (" (GEMM loads from host memory)" if args.zero_copy
+                                                                   else " (copy engine)"),
+                     "peak_source": "best pinned H2D copy of one pack, measured in this run before "
+                                    f"({link_before:.1f} GB/s) and after ({link_after:.1f} GB/s) the timed prefills"},
         "layer_roofline": {"t_roof_ms": t_roof_ms, "frac": t_roof_ms / ms},
+        "per_layer": {"copy_ms_mean": float(np.mean(copy_ms)) if copy_ms else None,
+                      "compute_ms_mean": float(np.mean(comp_ms)) if comp_ms else None,
+                      "copy_ms": copy_ms, "compute_ms": comp_ms, "span_ms": per_layer["span_ms"],
+                      "note": "CUDA events the library records on the copy and compute streams, last timed prefill"},
         "serialized_control_ms": ms_serial,
     }
 
@@ -540,28 +592,38 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="dsv4", choices=sorted(syn.CONFIGS))
+    ap.add_argument("--workload", default="kimi_T8192", choices=sorted(syn.CONFIGS))
+    ap.add_argument("--secondary", default="dsv4", help="a second workload measured after the first and nested "
+                                                          "under 'secondary' ('none' to skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget-s", type=float, default=150.0)
     ap.add_argument("--layer-stores", type=int, default=4,
                     help="layerwise workload: distinct pinned host layer stores, cycled over the layers")
+    ap.add_argument("--zero-copy", action="store_true",
+                    help="layerwise workload: the GEMMs read each layer's experts in place from pinned host memory")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.gpus != 1 or world != 1:
+        # one GPU only: the layer is not sharded and has no collective step
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "impl": args.impl, "n_gpus": max(args.gpus, world),
+                              "unavailable": "single-GPU only: the MoE layer runs on one GPU with no sharding and "
+                                             "no collective; multi-GPU runs are out of scope"}), flush=True)
+        return
     cfg = syn.CONFIGS[args.workload]
-    world, rank, local = dist_setup(args)
     if args.impl == "reference":
-        res = run_reference(args, cfg, world, rank)
+        res = run_reference(args, cfg)
     elif cfg.layers > 1:
-        res = run_layerwise(args, cfg, world, rank, local)
+        res = run_layerwise(args, cfg)
     else:
-        res = run_ours(args, cfg, world, rank, local)
-    if rank == 0 and res is not None:
-        print(json.dumps(res), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.destroy_process_group()
+        res = run_ours(args, cfg)
+        if args.secondary not in ("none", "", args.workload):
+            res["secondary"] = {args.secondary: secondary_summary(run_ours(args, syn.CONFIGS[args.secondary],
+                                                                           full=False))}
+    print(json.dumps(res), flush=True)
 
 
 if __name__ == "__main__":

@@ -126,14 +126,17 @@ kt_status kt_moe_route_permute(const float* logits, int T, int E, int k, int ren
  * file-scope device array of KT_NOALLOC_SCRATCH_BYTES inside the library,
  * which every GPU that loads the library holds until the process exits.
  *   - Arguments, outputs, limits and errors as for kt_moe_route_permute,
- *     without ws/ws_bytes.  Sizes whose scratch need
+ *     without ws/ws_bytes, checked in the same order (shape, null
+ *     pointers, alignment).  Then sizes whose scratch need
  *     (kt_moe_route_workspace_bytes(T, E, k)) exceeds
  *     KT_NOALLOC_SCRATCH_BYTES return KT_ERR_WORKSPACE before anything runs
  *     (1 MiB covers, e.g., T = 8192 tokens with E = 896, k = 16).
  *   - It calls no cudaMalloc, cudaFree or other allocating routine.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture on the device.
+ *   - Every call looks up the array's device address in the current
+ *     device's context (cudaGetSymbolAddress, a host-side lookup), so the
+ *     address stays right after a context reset.  The first call on a
+ *     device may also load the library's device code into that context;
+ *     make that first call before any stream capture on the device.
  *   - All calls share the one array and leave their scratch in it; each call
  *     clears the error word it uses and fully rewrites the rest before
  *     reading it.  Calls that overlap on the GPU (other streams, other host
@@ -322,8 +325,41 @@ kt_status kt_layerwise_create(kt_layerwise** ctx, int L, int H, int I, int E, in
 kt_status kt_layerwise_prefill(kt_layerwise* ctx, const uint16_t* hidden, const float* const* logits,
                                uint16_t* out, int T, int serialized_control, void* stream);
 
+/*
+ * Zero-copy variant of kt_layerwise_create for hosts whose memory the GPU
+ * reads coherently (a Grace-Blackwell node over NVLink-C2C).  Same arguments;
+ * each host_packs[l] must be pinned (cudaHostAlloc or cudaHostRegister) and
+ * 256-byte aligned.  No device slots and no copy stream traffic: in
+ * kt_layerwise_prefill the GEMMs of layer l read its packed experts in place
+ * from host_packs[l] (through its device address, cudaHostGetDevicePointer),
+ * so the host link is crossed by the GEMM's own loads.  Everything else
+ * (workspace, routing buffers, hidden ping-pong buffers) is as for
+ * kt_layerwise_create.  Errors: KT_ERR_INVALID_ARG when a pack is not pinned,
+ * not mapped or misaligned; otherwise as kt_layerwise_create.
+ * This is the zero-copy form of the double-buffered layerwise prefill that
+ * issue 2172 (Background / motivation) asks for in place of the per-layer
+ * "load -> compute -> sync" chain of its Impact section.
+ */
+kt_status kt_layerwise_create_zero_copy(kt_layerwise** ctx, int L, int H, int I, int E, int k, int T_max,
+                                        const void* const* host_packs);
+
+/*
+ * Per-layer timing of the next prefills (measurement hook).  enable = 1
+ * creates 4*L+1 CUDA events; every later kt_layerwise_prefill records, per
+ * layer, events around its copy (on the copy stream) and around its compute
+ * (routing + forward, on the caller's stream), plus one start event.
+ * kt_layerwise_read_timing synchronises on the last layer's events and
+ * writes, for the most recent prefill: copy_ms[l] and compute_ms[l] (HOST
+ * arrays of L doubles, milliseconds; copy_ms is 0 in zero-copy mode) and
+ * *span_ms, the time from the start event to the end of the last layer.
+ * enable = 0 frees the events.  Not thread-safe.
+ */
+kt_status kt_layerwise_enable_timing(kt_layerwise* ctx, int enable);
+kt_status kt_layerwise_read_timing(kt_layerwise* ctx, double* copy_ms, double* compute_ms, double* span_ms);
+
 /* Test hook: make the copy step of layer `layer` report KT_ERR_CUDA
- * (-1 disables).  The pipeline must drain both streams and return it. */
+ * (-1 disables).  The pipeline must drain both streams and return it.
+ * In zero-copy mode the same layer's step reports it before its compute. */
 kt_status kt_layerwise_inject_copy_failure(kt_layerwise* ctx, int layer);
 
 kt_status kt_layerwise_destroy(kt_layerwise* ctx);

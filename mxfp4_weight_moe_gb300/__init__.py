@@ -68,6 +68,10 @@ _SIGNATURES = {
     "kt_layerwise_create": ([ctypes.POINTER(_VP), _I, _I, _I, _I, _I, _I, ctypes.POINTER(_VP)], _I),
     "kt_layerwise_prefill": ([_VP, _VP, ctypes.POINTER(_VP), _VP, _I, _I, _VP], _I),
     "kt_layerwise_inject_copy_failure": ([_VP, _I], _I),
+    "kt_layerwise_create_zero_copy": ([ctypes.POINTER(_VP), _I, _I, _I, _I, _I, _I, ctypes.POINTER(_VP)], _I),
+    "kt_layerwise_enable_timing": ([_VP, _I], _I),
+    "kt_layerwise_read_timing": ([_VP, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(ctypes.c_double)], _I),
     "kt_layerwise_destroy": ([_VP], _I),
     "kt_moe_kernel_launches": ([], ctypes.c_uint64),
     "kt_moe_profile_enable": ([_I], _I),
@@ -318,18 +322,35 @@ def profile_read() -> dict:
 class Layerwise:
     """Layerwise prefill over L layers whose packed experts live in pinned host memory."""
 
-    def __init__(self, host_packs: list[torch.Tensor], H: int, I: int, E: int, k: int, T_max: int):
+    def __init__(self, host_packs: list[torch.Tensor], H: int, I: int, E: int, k: int, T_max: int,
+                 zero_copy: bool = False):
+        """zero_copy=False: two device slots, the next layer copied while the current one computes.
+        zero_copy=True: the GEMMs read each layer's experts in place from the pinned host packs."""
         self.H, self.I, self.E, self.k, self.T_max = H, I, E, k, T_max
+        self.zero_copy = bool(zero_copy)
         need = int(lib().kt_layerwise_pack_bytes(H, I, E))
         for p in host_packs:
             if p.device.type != "cpu" or not p.is_pinned() or p.dtype != torch.uint8 or p.numel() < need:
                 raise ValueError(f"each host pack must be a pinned uint8 CPU tensor of >= {need} bytes")
         self._packs = list(host_packs)     # keep them alive
+        self.L = len(host_packs)
         arr = (ctypes.c_void_p * len(host_packs))(*[p.data_ptr() for p in host_packs])
         h = ctypes.c_void_p()
-        _check(lib().kt_layerwise_create(ctypes.byref(h), len(host_packs), H, I, E, k, T_max, arr),
-               "kt_layerwise_create")
+        create = lib().kt_layerwise_create_zero_copy if self.zero_copy else lib().kt_layerwise_create
+        _check(create(ctypes.byref(h), len(host_packs), H, I, E, k, T_max, arr), "kt_layerwise_create")
         self._h = h
+
+    def enable_timing(self, enable: bool = True):
+        """Record per-layer copy / compute events in the following prefills."""
+        _check(lib().kt_layerwise_enable_timing(self._h, int(bool(enable))), "kt_layerwise_enable_timing")
+
+    def timing(self) -> dict:
+        """{"layers": [(copy_ms, compute_ms)] per layer, "span_ms": ...} of the most recent prefill."""
+        cp = (ctypes.c_double * self.L)()
+        cm = (ctypes.c_double * self.L)()
+        span = ctypes.c_double()
+        _check(lib().kt_layerwise_read_timing(self._h, cp, cm, ctypes.byref(span)), "kt_layerwise_read_timing")
+        return {"layers": [(float(cp[i]), float(cm[i])) for i in range(self.L)], "span_ms": float(span.value)}
 
     @staticmethod
     def pack_bytes(H: int, I: int, E: int) -> int:

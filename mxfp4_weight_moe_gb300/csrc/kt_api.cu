@@ -100,6 +100,18 @@ static kt_status check_route_shape(int T, int E, int k) {
     return KT_OK;
 }
 
+kt_status check_route_args(const float* logits, int T, int E, int k, const int32_t* topk_ids, const float* topk_w,
+                           const int32_t* expert_offsets, const int32_t* perm, const int32_t* inv_perm) {
+    kt_status st = check_route_shape(T, E, k);
+    if (st != KT_OK || T == 0) return st;
+    if (!logits || !topk_ids || !topk_w || !expert_offsets || !perm || !inv_perm)
+        return fail(KT_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(expert_offsets, 4) ||
+        !aligned(perm, 4) || !aligned(inv_perm, 4))
+        return fail(KT_ERR_ALIGNMENT, "routing pointers must be 4-byte aligned");
+    return KT_OK;
+}
+
 }  // namespace kt
 
 using namespace kt;
@@ -133,14 +145,9 @@ kt_status kt_moe_route_permute(const float* logits, int T, int E, int k, int ren
                                float* topk_w, int32_t* expert_offsets, int32_t* perm, int32_t* inv_perm, void* ws,
                                size_t ws_bytes, void* stream) {
     g_last_error[0] = '\0';
-    kt_status st = check_route_shape(T, E, k);
-    if (st != KT_OK) return st;
-    if (T == 0) return KT_OK;
-    if (!logits || !topk_ids || !topk_w || !expert_offsets || !perm || !inv_perm || !ws)
-        return fail(KT_ERR_INVALID_ARG, "null pointer argument");
-    if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(expert_offsets, 4) ||
-        !aligned(perm, 4) || !aligned(inv_perm, 4))
-        return fail(KT_ERR_ALIGNMENT, "routing pointers must be 4-byte aligned");
+    kt_status st = check_route_args(logits, T, E, k, topk_ids, topk_w, expert_offsets, perm, inv_perm);
+    if (st != KT_OK || T == 0) return st;
+    if (!ws) return fail(KT_ERR_INVALID_ARG, "null pointer argument");
     RouteWs L;
     route_ws_layout(T, E, k, &L);
     if (!aligned(ws, 256)) return fail(KT_ERR_WORKSPACE, "workspace must be 256-byte aligned");

@@ -130,6 +130,12 @@ kt_status launch_gemm(const GemmArgs& a, cudaStream_t s);
 // Device properties cached per device.
 int sm_count();
 
+// Argument checks of the routing entry points (shape limits, null pointers,
+// 4-byte alignment), in that order; KT_OK also for T == 0.  Records the
+// failing check as kt_last_error().
+kt_status check_route_args(const float* logits, int T, int E, int k, const int32_t* topk_ids, const float* topk_w,
+                           const int32_t* expert_offsets, const int32_t* perm, const int32_t* inv_perm);
+
 // Status helper: map a CUDA error to KT_ERR_CUDA, remembering the last one.
 kt_status cuda_status(cudaError_t e);
 // Record `msg` as this thread's kt_last_error() text and return `st`.

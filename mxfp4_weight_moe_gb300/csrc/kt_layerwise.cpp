@@ -12,6 +12,16 @@
 //   copy(l+1) into slot (l+1)%2 waits for consumed[(l+1)%2] (layer l-1 done)
 //   compute(l) waits for copied[l%2]
 // Host-side waits poll with a deadline and return KT_ERR_TIMEOUT.
+//
+// Zero-copy mode (a GB300 node's Grace host memory is coherent with the GPU
+// over NVLink-C2C): no device slots and no copies; each layer's GEMMs read
+// its packed experts in place from the pinned host pack, through the host
+// pack's device address.  Only host memory that this process pinned is
+// read; nothing is multicast.
+//
+// Optional per-layer timing: events on the copy stream around each layer's
+// copy and on the compute stream around each layer's compute, read back by
+// kt_layerwise_read_timing.
 #include <chrono>
 #include <cstring>
 #include <new>
@@ -41,6 +51,10 @@ struct kt_layerwise {
     int32_t* perm = nullptr;
     int32_t* inv_perm = nullptr;
     int inject_layer = -1;
+    int zero_copy = 0;
+    std::vector<const void*> dev_packs;   // zero-copy: device addresses of the host packs
+    bool timing = false;
+    std::vector<cudaEvent_t> ev;          // timing: [copy_b, copy_e, comp_b, comp_e] per layer, then start
 };
 
 namespace {
@@ -73,8 +87,15 @@ void pack_offsets(int H, int I, int E, size_t* o13, size_t* o13s, size_t* o2, si
     *total = off;
 }
 
+void free_timing(kt_layerwise* c) {
+    for (cudaEvent_t e : c->ev)
+        if (e) cudaEventDestroy(e);
+    c->ev.clear();
+}
+
 void free_ctx(kt_layerwise* c) {
     if (!c) return;
+    free_timing(c);
     for (int i = 0; i < 2; ++i) {
         if (c->slot[i]) cudaFree(c->slot[i]);
         if (c->hbuf[i]) cudaFree(c->hbuf[i]);
@@ -112,8 +133,8 @@ kt_status kt_layerwise_pack_offsets(int H, int I, int E, size_t* w13, size_t* w1
     return KT_OK;
 }
 
-kt_status kt_layerwise_create(kt_layerwise** out, int L, int H, int I, int E, int k, int T_max,
-                              const void* const* host_packs) {
+static kt_status create_ctx(kt_layerwise** out, int L, int H, int I, int E, int k, int T_max,
+                            const void* const* host_packs, int zero_copy) {
     if (!out || !host_packs || L <= 0 || T_max <= 0) return KT_ERR_INVALID_ARG;
     *out = nullptr;
     if (kt_moe_workspace_bytes(T_max, H, I, E, k) == 0) return KT_ERR_UNSUPPORTED_SHAPE;
@@ -129,14 +150,29 @@ kt_status kt_layerwise_create(kt_layerwise** out, int L, int H, int I, int E, in
     c->k = k;
     c->T_max = T_max;
     c->inject_layer = -1;
+    c->zero_copy = zero_copy ? 1 : 0;
     cudaGetDevice(&c->dev);
     pack_offsets(H, I, E, &c->off_w13, &c->off_w13_sf, &c->off_w2, &c->off_w2_sf, &c->pack_bytes);
     c->ws_bytes = kt_moe_workspace_bytes(T_max, H, I, E, k);
     c->route_ws_bytes = kt_moe_route_workspace_bytes(T_max, E, k);
     const size_t S = static_cast<size_t>(T_max) * k;
     bool ok = true;
+    if (c->zero_copy) {
+        // the device address of each pinned host pack (fails for memory that is not pinned)
+        for (int l = 0; l < L && ok; ++l) {
+            void* d = nullptr;
+            const cudaError_t e = cudaHostGetDevicePointer(&d, const_cast<void*>(host_packs[l]), 0);
+            if (e != cudaSuccess || d == nullptr || (reinterpret_cast<uintptr_t>(d) & 255u) != 0) {
+                cudaGetLastError();
+                free_ctx(c);
+                return kt::report(KT_ERR_INVALID_ARG,
+                                  "zero-copy layerwise needs pinned, device-mapped, 256-byte aligned host packs");
+            }
+            c->dev_packs.push_back(d);
+        }
+    }
     for (int i = 0; i < 2 && ok; ++i) {
-        ok = ok && cudaMalloc(&c->slot[i], c->pack_bytes) == cudaSuccess;
+        if (!c->zero_copy) ok = ok && cudaMalloc(&c->slot[i], c->pack_bytes) == cudaSuccess;
         ok = ok && cudaMalloc(reinterpret_cast<void**>(&c->hbuf[i]), sizeof(uint16_t) * T_max * H) == cudaSuccess;
         ok = ok && cudaEventCreateWithFlags(&c->copied[i], cudaEventDisableTiming) == cudaSuccess;
         ok = ok && cudaEventCreateWithFlags(&c->consumed[i], cudaEventDisableTiming) == cudaSuccess;
@@ -158,6 +194,57 @@ kt_status kt_layerwise_create(kt_layerwise** out, int L, int H, int I, int E, in
     return KT_OK;
 }
 
+kt_status kt_layerwise_create(kt_layerwise** out, int L, int H, int I, int E, int k, int T_max,
+                              const void* const* host_packs) {
+    return create_ctx(out, L, H, I, E, k, T_max, host_packs, 0);
+}
+
+kt_status kt_layerwise_create_zero_copy(kt_layerwise** out, int L, int H, int I, int E, int k, int T_max,
+                                        const void* const* host_packs) {
+    return create_ctx(out, L, H, I, E, k, T_max, host_packs, 1);
+}
+
+kt_status kt_layerwise_enable_timing(kt_layerwise* c, int enable) {
+    if (!c) return KT_ERR_INVALID_ARG;
+    free_timing(c);
+    c->timing = false;
+    if (!enable) return KT_OK;
+    c->ev.assign(static_cast<size_t>(4 * c->L + 1), nullptr);
+    for (auto& e : c->ev) {
+        if (cudaEventCreate(&e) != cudaSuccess) {
+            const cudaError_t err = cudaGetLastError();
+            free_timing(c);
+            return kt::cuda_status(err);
+        }
+    }
+    c->timing = true;
+    return KT_OK;
+}
+
+kt_status kt_layerwise_read_timing(kt_layerwise* c, double* copy_ms, double* compute_ms, double* span_ms) {
+    if (!c || !copy_ms || !compute_ms || !span_ms) return KT_ERR_INVALID_ARG;
+    if (!c->timing) return kt::report(KT_ERR_INVALID_ARG, "timing is not enabled");
+    kt_status st;
+    const cudaEvent_t start = c->ev[4 * c->L];
+    float last = 0.f;
+    for (int l = 0; l < c->L; ++l) {
+        float a = 0.f, b = 0.f, e_end = 0.f;
+        if ((st = kt::cuda_status(cudaEventSynchronize(c->ev[4 * l + 3]))) != KT_OK) return st;
+        if (c->zero_copy) {
+            copy_ms[l] = 0.0;
+        } else {
+            if ((st = kt::cuda_status(cudaEventElapsedTime(&a, c->ev[4 * l], c->ev[4 * l + 1]))) != KT_OK) return st;
+            copy_ms[l] = a;
+        }
+        if ((st = kt::cuda_status(cudaEventElapsedTime(&b, c->ev[4 * l + 2], c->ev[4 * l + 3]))) != KT_OK) return st;
+        compute_ms[l] = b;
+        if ((st = kt::cuda_status(cudaEventElapsedTime(&e_end, start, c->ev[4 * l + 3]))) != KT_OK) return st;
+        if (e_end > last) last = e_end;
+    }
+    *span_ms = last;
+    return KT_OK;
+}
+
 kt_status kt_layerwise_inject_copy_failure(kt_layerwise* c, int layer) {
     if (!c) return KT_ERR_INVALID_ARG;
     c->inject_layer = layer;
@@ -169,21 +256,27 @@ static kt_status enqueue_copy(kt_layerwise* c, int l, cudaStream_t s, bool wait_
     const int b = l & 1;
     kt_status st;
     if (wait_consumed && (st = kt::cuda_status(cudaStreamWaitEvent(s, c->consumed[b], 0))) != KT_OK) return st;
+    if (c->timing && (st = kt::cuda_status(cudaEventRecord(c->ev[4 * l], s))) != KT_OK) return st;
     if ((st = kt::cuda_status(cudaMemcpyAsync(c->slot[b], c->host_packs[l], c->pack_bytes, cudaMemcpyHostToDevice,
                                               s))) != KT_OK)
         return st;
+    if (c->timing && (st = kt::cuda_status(cudaEventRecord(c->ev[4 * l + 1], s))) != KT_OK) return st;
     return kt::cuda_status(cudaEventRecord(c->copied[b], s));
 }
 
 static kt_status compute_layer(kt_layerwise* c, int l, const uint16_t* in, const float* logits, uint16_t* outp,
                                int T, cudaStream_t s) {
     const int b = l & 1;
-    const uint8_t* base = static_cast<const uint8_t*>(c->slot[b]);
-    kt_status st = kt_moe_route_permute(logits, T, c->E, c->k, 1, c->ids, c->w, c->offsets, c->perm, c->inv_perm,
+    const uint8_t* base = static_cast<const uint8_t*>(c->zero_copy ? c->dev_packs[l] : c->slot[b]);
+    kt_status st;
+    if (c->timing && (st = kt::cuda_status(cudaEventRecord(c->ev[4 * l + 2], s))) != KT_OK) return st;
+    st = kt_moe_route_permute(logits, T, c->E, c->k, 1, c->ids, c->w, c->offsets, c->perm, c->inv_perm,
                                         c->route_ws, c->route_ws_bytes, s);
     if (st != KT_OK) return st;
-    return kt_mxfp4_moe_forward(in, T, c->H, c->ids, c->w, c->k, base + c->off_w13, base + c->off_w13_sf,
-                                base + c->off_w2, base + c->off_w2_sf, c->E, c->I, outp, c->ws, c->ws_bytes, s);
+    st = kt_mxfp4_moe_forward(in, T, c->H, c->ids, c->w, c->k, base + c->off_w13, base + c->off_w13_sf,
+                              base + c->off_w2, base + c->off_w2_sf, c->E, c->I, outp, c->ws, c->ws_bytes, s);
+    if (st == KT_OK && c->timing) st = kt::cuda_status(cudaEventRecord(c->ev[4 * l + 3], s));
+    return st;
 }
 
 kt_status kt_layerwise_prefill(kt_layerwise* c, const uint16_t* hidden, const float* const* logits, uint16_t* out,
@@ -194,10 +287,21 @@ kt_status kt_layerwise_prefill(kt_layerwise* c, const uint16_t* hidden, const fl
     if (T == 0) return KT_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     kt_status st = KT_OK;
+    if (c->timing) {
+        // the copy stream's first copy and the compute stream's first layer both follow this event
+        st = kt::cuda_status(cudaEventRecord(c->ev[4 * c->L], s));
+        if (st == KT_OK && !c->zero_copy) st = kt::cuda_status(cudaStreamWaitEvent(c->copy_stream, c->ev[4 * c->L], 0));
+        if (st != KT_OK) return st;
+    }
     for (int l = 0; l < c->L && st == KT_OK; ++l) {
         const uint16_t* in = (l == 0) ? hidden : c->hbuf[(l - 1) & 1];
         uint16_t* o = (l == c->L - 1) ? out : c->hbuf[l & 1];
-        if (serialized_control) {
+        if (c->zero_copy) {
+            // the GEMMs read the layer's experts in place: no copy and no slot to wait for
+            if (l == c->inject_layer) st = KT_ERR_CUDA;
+            if (st == KT_OK) st = compute_layer(c, l, in, logits[l], o, T, s);
+            if (st == KT_OK && serialized_control) st = wait_stream(s);
+        } else if (serialized_control) {
             // upload all experts -> compute -> synchronise, one layer at a time
             st = enqueue_copy(c, l, s, false);
             if (st == KT_OK) st = compute_layer(c, l, in, logits[l], o, T, s);

@@ -15,6 +15,7 @@ import oracle as O
 from mxfp4_weight_moe_gb300 import synthetic as syn
 
 from helpers import OUT_RTOL, bf16_bits_np, bf16_to_f64, check_a2, normwise_rel, oracle_subset, sample_tokens, \
+    scale_flips_valid, \
     ws_view
 
 pytestmark = pytest.mark.gpu
@@ -82,6 +83,8 @@ def _check_case(hidden, ids_np, w_np, W, tokens=None, check_a=True):
                 gc.append(a2[p]); gs.append(a2_sf[p]); rc2.append(ref["a2"][i, j]); rs2.append(ref["a2_sf"][i, j])
         frac, worst = check_a2(np.array(gc), np.array(gs), np.array(rc2), np.array(rs2))
         assert frac <= 1e-3 and worst <= 1.0 + 1e-9, (frac, worst)
+        n_sf, bad_sf = scale_flips_valid(np.array(gc), np.array(gs), np.array(rc2), np.array(rs2))
+        assert bad_sf == 0, f"{bad_sf} of {n_sf} A2 scale differences are not a power-of-two straddle"
     got = bf16_to_f64(bf16_bits_np(out)[tokens])
     rel = normwise_rel(got, ref["out_f64"])
     assert rel.max() <= OUT_RTOL, f"max normwise rel err {rel.max():.3e} at token {tokens[int(rel.argmax())]}"

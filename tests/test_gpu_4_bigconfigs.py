@@ -16,7 +16,7 @@ from test_gpu_3_forward import _check_case
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
-@pytest.mark.parametrize("name,n_sample", [("dsv4", 96), ("kimi_T16", 16), ("kimi_T8192", 12)])
+@pytest.mark.parametrize("name,n_sample", [("dsv4", 256), ("kimi_T16", 16), ("kimi_T8192", 64)])
 def test_full_size_config(name, n_sample):
     cfg = syn.CONFIGS[name]
     hidden = syn.make_hidden(cfg.T, cfg.H, cfg.seed, device="cuda")

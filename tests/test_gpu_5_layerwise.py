@@ -86,3 +86,72 @@ def test_layerwise_copy_failure_is_reported_and_recoverable():
         assert torch.equal(again.view(torch.int16), ref.view(torch.int16))
     finally:
         lw.close()
+
+
+def test_layerwise_timing_hook_reports_every_layer():
+    weights, packs, logits = _layers()
+    hidden = syn.make_hidden(T, H, 0, device="cuda")
+    lw = kt.Layerwise(packs, H, I, E, K, T_max=T)
+    try:
+        lw.enable_timing(True)
+        lw.prefill(hidden, logits)
+        t = lw.timing()
+        lw.enable_timing(False)
+    finally:
+        lw.close()
+    assert len(t["layers"]) == L
+    for copy_ms, compute_ms in t["layers"]:
+        assert copy_ms > 0 and compute_ms > 0
+    assert t["span_ms"] >= max(c for _, c in t["layers"])
+
+
+@pytest.mark.slow
+def test_layerwise_dsv4_shaped_three_layers_match_per_layer_forwards():
+    # the DeepSeek-V4-Flash-shaped layer (H=4096, E=256, top-6, I=2048) that the 43-layer workload streams
+    Ld, Td, Hd, Id, Ed, Kd = 3, 512, 4096, 2048, 256, 6
+    hidden = syn.make_hidden(Td, Hd, 0, device="cuda")
+    logits = [syn.make_logits(Td, Ed, "zipf", seed=l, device="cuda") for l in range(Ld)]
+    packs = []
+    for l in range(Ld):
+        W = syn.make_weights(Ed, Hd, Id, seed=1000 * l, device="cuda")
+        packs.append(kt.Layerwise.pack(*[t.cpu() for t in W]))
+        del W
+    lw = kt.Layerwise(packs, Hd, Id, Ed, Kd, T_max=Td)
+    try:
+        streamed = lw.prefill(hidden, logits).clone()
+        torch.cuda.synchronize()
+    finally:
+        lw.close()
+    off = kt.Layerwise.pack_offsets(Hd, Id, Ed)
+    shapes = ((Ed, 2 * Id, Hd // 2), (Ed, 2 * Id, Hd // 32), (Ed, Hd, Id // 2), (Ed, Hd, Id // 32))
+    h = hidden
+    for l in range(Ld):
+        dev_pack = packs[l].cuda()
+        W = [dev_pack[o:o + int(np.prod(s))].view(*s) for o, s in zip(off, shapes)]
+        ids, w, *_ = kt.route_permute(logits[l], Kd)
+        h = kt.forward(h, ids, w, *W)
+        torch.cuda.synchronize()
+        del W, dev_pack
+    assert torch.equal(streamed.view(torch.int16), h.view(torch.int16))
+
+
+def test_layerwise_zero_copy_matches_streamed():
+    # the GEMMs read each layer's experts in place from the pinned host packs: results are those of the
+    # double-buffered device-slot schedule, bit for bit
+    weights, packs, logits = _layers()
+    hidden = syn.make_hidden(T, H, 0, device="cuda")
+    lw = kt.Layerwise(packs, H, I, E, K, T_max=T)
+    zc = kt.Layerwise(packs, H, I, E, K, T_max=T, zero_copy=True)
+    try:
+        ref = lw.prefill(hidden, logits).clone()
+        zc.enable_timing(True)
+        got = zc.prefill(hidden, logits).clone()
+        t = zc.timing()
+        serial = zc.prefill(hidden, logits, serialized=True).clone()
+        torch.cuda.synchronize()
+    finally:
+        lw.close()
+        zc.close()
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(serial.view(torch.int16), ref.view(torch.int16))
+    assert all(c == 0.0 and m > 0 for c, m in t["layers"])
