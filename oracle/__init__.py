@@ -84,6 +84,9 @@ def lib():
                 c_u8p, c_u8p, c_u8p, c_u8p, ctypes.c_int, ctypes.c_int,
                 c_i32p, ctypes.c_int, c_u16p, c_f64p, c_u8p, c_u8p, c_f64p, ctypes.c_int]
             L.mxo_moe_forward_tokens.restype = ctypes.c_int
+            L.mxo_moe_forward_tokens_ex.argtypes = L.mxo_moe_forward_tokens.argtypes + [
+                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double]
+            L.mxo_moe_forward_tokens_ex.restype = ctypes.c_int
             L.mxo_max_threads.argtypes = []
             L.mxo_max_threads.restype = ctypes.c_int
             _lib = L
@@ -217,9 +220,21 @@ def check_fc_shapes(w13: np.ndarray, w2: np.ndarray):
     return E, fc2_inter, H
 
 
+GATE_UP_LAYOUTS = ("halves", "interleaved")
+ACTIVATIONS = ("swiglu", "swiglu_clamped")
+
+
 def moe_forward(hidden_bits: np.ndarray, ids: np.ndarray, topk_w: np.ndarray,
-                w13, w13_sf, w2, w2_sf, tokens=None, want=("out",), nthreads: int = 0):
+                w13, w13_sf, w2, w2_sf, tokens=None, want=("out",), nthreads: int = 0,
+                gate_up: str = "halves", activation: str = "swiglu", alpha: float = 1.702, limit: float = 7.0):
     """The whole layer for the listed tokens (default: all).
+
+    gate_up: "halves" (w13 rows [0, I) gate, [I, 2I) up) or "interleaved"
+    (row 2i gate, row 2i+1 up).  activation: "swiglu" (silu(g) * u) or
+    "swiglu_clamped" (min(g, limit) * sigmoid(alpha * min(g, limit)) *
+    (clamp(u, -limit, limit) + 1), the gated activation of GPT-OSS-format
+    checkpoints, whose SwiGLU weight layout and parameters "Kimi-K3 SM120
+    FlashInfer MXFP4 MoE", Phase 0 audit conclusions, item 4, names).
 
     Returns a dict with any of: "out" (bf16 bits [n, H]), "out_f64" [n, H],
     "a2" (e4m3 [n, k, I]), "a2_sf" ([n, k, I/32]), "y" (fp64 [n, k, H])."""
@@ -239,12 +254,13 @@ def moe_forward(hidden_bits: np.ndarray, ids: np.ndarray, topk_w: np.ndarray,
     a2 = np.empty((n, k, I), np.uint8) if "a2" in want else None
     a2_sf = np.empty((n, k, I // 32), np.uint8) if "a2_sf" in want else None
     y = np.empty((n, k, H), np.float64) if "y" in want else None
-    _check(lib().mxo_moe_forward_tokens(
+    _check(lib().mxo_moe_forward_tokens_ex(
         _ptr(hidden_bits, ctypes.c_uint16), T, H, _ptr(ids, ctypes.c_int32), _ptr(topk_w, ctypes.c_float), k,
         _ptr(w13, ctypes.c_uint8), _ptr(w13_sf, ctypes.c_uint8), _ptr(w2, ctypes.c_uint8),
         _ptr(w2_sf, ctypes.c_uint8), E, I, _ptr(tokens, ctypes.c_int32), n,
         _ptr(out, ctypes.c_uint16), _ptr(out_f64, ctypes.c_double), _ptr(a2, ctypes.c_uint8),
-        _ptr(a2_sf, ctypes.c_uint8), _ptr(y, ctypes.c_double), int(nthreads)), "moe_forward")
+        _ptr(a2_sf, ctypes.c_uint8), _ptr(y, ctypes.c_double), int(nthreads),
+        GATE_UP_LAYOUTS.index(gate_up), ACTIVATIONS.index(activation), float(alpha), float(limit)), "moe_forward")
     for name, arr in (("out", out), ("out_f64", out_f64), ("a2", a2), ("a2_sf", a2_sf), ("y", y)):
         if arr is not None:
             res[name] = arr

@@ -28,7 +28,12 @@
  *    the full softmax over all E logits taken at the selected experts.
  *  - permutation: rows grouped by expert, stable in slot order s = t*k + j.
  *  - w13 rows [0, I) are the gate projection, rows [I, 2I) the up projection;
- *    SwiGLU h = silu(gate) * up with no clamp, alpha or bias.
+ *    SwiGLU h = silu(gate) * up with no clamp, alpha or bias.  As an option,
+ *    the gate/up rows interleave (row 2i gate, row 2i+1 up) and the gated
+ *    activation is the clamped SwiGLU of GPT-OSS-format checkpoints ("Kimi-K3
+ *    SM120 FlashInfer MXFP4 MoE", Phase 0 audit conclusions, item 4, names
+ *    that model's SwiGLU weight layout and parameters without stating them;
+ *    the definition below is the published GPT-OSS one).
  *  - FC1 accumulators and h are not rounded before the MXFP8 requant.
  *  - the routing weight multiplies the FC2 output (not folded into A2).
  *  - all arithmetic is fp64; the output is rounded once to bf16 (RNE).
@@ -335,11 +340,27 @@ int mxo_gemm_mxfp8_mxfp4(const uint8_t* a, const uint8_t* a_sf, int M, int K,
 /* The MoE layer.                                                     */
 /* ------------------------------------------------------------------ */
 
+/* The gated activation of one FC1 output pair (gate g, up u):
+ *   act 0, SwiGLU:          h = silu(g) * u = g / (1 + e^-g) * u
+ *   act 1, clamped SwiGLU:  g' = min(g, limit), u' = min(max(u, -limit), limit),
+ *                           h = g' / (1 + e^(-alpha g')) * (u' + 1)
+ * (for GPT-OSS-format checkpoints alpha = 1.702 and limit = 7).  fp64. */
+static double gated_activation(double g, double u, int act, double alpha, double limit)
+{
+    if (act == 0) return g / (1.0 + exp(-g)) * u;
+    if (g > limit) g = limit;
+    if (u > limit) u = limit;
+    if (u < -limit) u = -limit;
+    return g / (1.0 + exp(-alpha * g)) * (u + 1.0);
+}
+
 /* Forward of the MoE layer for a list of tokens (each token's output depends
  * only on its own hidden row and routing, so a subset is exact):
  *   a      = MXFP8(hidden[t])                                  (per 32 along H)
  *   acc    = a . w13[e]^T   (2I outputs, block-scaled, fp64)
- *   h      = silu(acc[0:I]) * acc[I:2I]
+ *   h      = silu(acc[0:I]) * acc[I:2I]      (or, with gate_up_interleaved,
+ *            gate i = acc[2i], up i = acc[2i+1]; act selects the activation,
+ *            see gated_activation)
  *   a2     = MXFP8(h)                                          (per 32 along I)
  *   y      = a2 . w2[e]^T   (H outputs)
  *   out[t] = bf16( sum_j topk_w[t, j] * y(t, ids[t, j]) )
@@ -348,16 +369,18 @@ int mxo_gemm_mxfp8_mxfp4(const uint8_t* a, const uint8_t* a_sf, int M, int K,
  * nothing.  Optional outputs (NULL to skip), indexed by position in
  * `tokens`: out_f64 [n, H] (before bf16 rounding), a2 [n, k, I] and
  * a2_sf [n, k, I/32] (zero for skipped slots), y [n, k, H]. */
-int mxo_moe_forward_tokens(const uint16_t* hidden, int T, int H,
-                           const int32_t* ids, const float* topk_w, int k,
-                           const uint8_t* w13, const uint8_t* w13_sf,
-                           const uint8_t* w2, const uint8_t* w2_sf, int E, int I,
-                           const int32_t* tokens, int n_tokens,
-                           uint16_t* out, double* out_f64,
-                           uint8_t* a2_out, uint8_t* a2_sf_out, double* y_out, int nthreads)
+int mxo_moe_forward_tokens_ex(const uint16_t* hidden, int T, int H,
+                              const int32_t* ids, const float* topk_w, int k,
+                              const uint8_t* w13, const uint8_t* w13_sf,
+                              const uint8_t* w2, const uint8_t* w2_sf, int E, int I,
+                              const int32_t* tokens, int n_tokens,
+                              uint16_t* out, double* out_f64,
+                              uint8_t* a2_out, uint8_t* a2_sf_out, double* y_out, int nthreads,
+                              int gate_up_interleaved, int act, double alpha, double limit)
 {
     int ti, err = MXO_OK;
     if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || n_tokens < 0) return MXO_ERR_ARG;
+    if (act != 0 && act != 1) return MXO_ERR_ARG;
     if (H % 32 || I % 32) return MXO_ERR_SHAPE;
     if (!scales_finite(w13_sf, (size_t)E * 2 * I * (H / 32)) || !scales_finite(w2_sf, (size_t)E * H * (I / 32)))
         return MXO_ERR_NAN_SCALE;
@@ -403,8 +426,10 @@ int mxo_moe_forward_tokens(const uint16_t* hidden, int T, int H,
                     acc[n] = dot_mxfp8_mxfp4(av, sa, w13 + row * (H / 2), w13_sf + row * (H / 32), H);
                 }
                 for (i = 0; i < I; ++i) {
-                    double g = acc[i], u = acc[I + i];
-                    h[i] = g / (1.0 + exp(-g)) * u;
+                    double g, u;
+                    if (gate_up_interleaved) { g = acc[2 * i]; u = acc[2 * i + 1]; }
+                    else { g = acc[i]; u = acc[I + i]; }
+                    h[i] = gated_activation(g, u, act, alpha, limit);
                 }
                 mxo_quant_mxfp8(h, I, a2, sa2);
                 decode_e4m3_row(a2, I, a2v);
@@ -425,6 +450,19 @@ int mxo_moe_forward_tokens(const uint16_t* hidden, int T, int H,
         free(x); free(acc); free(h); free(sum); free(av); free(a2v); free(a); free(sa); free(a2); free(sa2);
     }
     return err;
+}
+
+/* The layer with the default gate | up halves and SwiGLU. */
+int mxo_moe_forward_tokens(const uint16_t* hidden, int T, int H,
+                           const int32_t* ids, const float* topk_w, int k,
+                           const uint8_t* w13, const uint8_t* w13_sf,
+                           const uint8_t* w2, const uint8_t* w2_sf, int E, int I,
+                           const int32_t* tokens, int n_tokens,
+                           uint16_t* out, double* out_f64,
+                           uint8_t* a2_out, uint8_t* a2_sf_out, double* y_out, int nthreads)
+{
+    return mxo_moe_forward_tokens_ex(hidden, T, H, ids, topk_w, k, w13, w13_sf, w2, w2_sf, E, I, tokens, n_tokens,
+                                     out, out_f64, a2_out, a2_sf_out, y_out, nthreads, 0, 0, 0.0, 0.0);
 }
 
 int mxo_max_threads(void)

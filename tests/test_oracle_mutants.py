@@ -15,7 +15,13 @@ SRC = os.path.join(ROOT, "oracle", "mx_oracle.c")
 
 MUTANTS = {
     "nibble_order": ("(kk & 1) ? (byte >> 4) : (byte & 15u)", "(kk & 1) ? (byte & 15u) : (byte >> 4)"),
-    "gate_up_swap": ("double g = acc[i], u = acc[I + i];", "double g = acc[I + i], u = acc[i];"),
+    "gate_up_swap": ("else { g = acc[i]; u = acc[I + i]; }", "else { g = acc[I + i]; u = acc[i]; }"),
+    "interleave_parity": ("{ g = acc[2 * i]; u = acc[2 * i + 1]; }", "{ g = acc[2 * i + 1]; u = acc[2 * i]; }"),
+    "clamp_gate_missing": ("    if (g > limit) g = limit;\n", ""),
+    "clamp_gate_symmetric": ("    if (g > limit) g = limit;\n", "    if (g > limit) g = limit;\n    if (g < -limit) g = -limit;\n"),
+    "clamp_up_missing": ("    if (u < -limit) u = -limit;\n", ""),
+    "up_offset_missing": ("* (u + 1.0);", "* u;"),
+    "alpha_missing": ("exp(-alpha * g)", "exp(-g)"),
     "e4m3_bias": ("ldexp(1.0 + (double)m / 8.0, (int)e - 7)", "ldexp(1.0 + (double)m / 8.0, (int)e - 8)"),
     "block_exponent_off_by_one": ("x = (e - 1) - emax_elem;", "x = e - emax_elem;"),
     "unstable_permutation": ("        perm[offsets[id] + fill[id]] = (int32_t)s;",
@@ -25,7 +31,7 @@ MUTANTS = {
     "e2m1_subnormal": ("0.5 * (double)m : ldexp", "1.0 * (double)m : ldexp"),
     "dropped_weight_scale": ("acc += mxo_e8m0_value(sa[b]) * mxo_e8m0_value(sw[b]) * blk;",
                              "acc += mxo_e8m0_value(sa[b]) * blk;"),
-    "silu_sign": ("h[i] = g / (1.0 + exp(-g)) * u;", "h[i] = g / (1.0 + exp(g)) * u;"),
+    "silu_sign": ("if (act == 0) return g / (1.0 + exp(-g)) * u;", "if (act == 0) return g / (1.0 + exp(g)) * u;"),
     "bf16_truncation": ("q = ldexp(rne_nonneg(ldexp(a, 7 - e)), e - 7);", "q = ldexp(floor(ldexp(a, 7 - e)), e - 7);"),
     "renormalize_ignored": ("        if (renormalize) {", "        if (1) {"),
     "e4m3_no_saturation": ("if (a >= 448.0) return sign | 0x7Eu;", "if (a > 464.0) return sign | 0x7Fu;"),

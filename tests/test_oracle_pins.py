@@ -89,8 +89,10 @@ def rand_weights(E, H, I, seed):
     return w13.numpy(), w13_sf.numpy(), w2.numpy(), w2_sf.numpy()
 
 
-def dense_layer(hidden_bits, ids, w, w13, w13_sf, w2, w2_sf, table):
-    """Brute force of the whole layer on dequantised dense matrices."""
+def dense_layer(hidden_bits, ids, w, w13, w13_sf, w2, w2_sf, table, gate_up="halves", activation="swiglu",
+                alpha=1.702, limit=7.0):
+    """Brute force of the whole layer on dequantised dense matrices (torch's
+    silu / clamp / sigmoid for the gated activation)."""
     T, H = hidden_bits.shape
     E, twoI, _ = w13.shape
     I = twoI // 2
@@ -107,8 +109,16 @@ def dense_layer(hidden_bits, ids, w, w13, w13_sf, w2, w2_sf, table):
             if e < 0 or e >= E:
                 continue
             acc = W13[e] @ a[t]
-            g, u = torch.from_numpy(acc[:I]), torch.from_numpy(acc[I:])
-            h = (torch.nn.functional.silu(g) * u).numpy()
+            if gate_up == "halves":
+                g, u = torch.from_numpy(acc[:I]), torch.from_numpy(acc[I:])
+            else:
+                g, u = torch.from_numpy(acc[0::2].copy()), torch.from_numpy(acc[1::2].copy())
+            if activation == "swiglu":
+                h = (torch.nn.functional.silu(g) * u).numpy()
+            else:
+                gc = torch.clamp(g, max=limit)
+                uc = torch.clamp(u, min=-limit, max=limit)
+                h = (gc * torch.sigmoid(alpha * gc) * (uc + 1.0)).numpy()
             c2, s2 = mxfp8_ref(h)
             a2s[t, j] = c2
             y = W2[e] @ mx_dequant_e4m3(c2, s2)
@@ -473,3 +483,93 @@ def test_fc1_is_twice_fc2_inter(golden_dir):
         O.check_fc_shapes(np.zeros((E, fc2, H // 2), np.uint8), w2)      # non-gated 128 rows
     cfg = syn.CONFIGS["tiny"]
     assert (cfg.T, cfg.H, cfg.E, cfg.k, cfg.I) == (T, H, E, k, I)
+
+
+# ------------------------------------------------------------ gate/up layout and activation variants
+# The interleaved gate/up rows and the clamped SwiGLU of GPT-OSS-format checkpoints ("Kimi-K3 SM120
+# FlashInfer MXFP4 MoE", Phase 0 audit conclusions, item 4): w13 row 2i is gate i and row 2i+1 up i;
+# h = min(g, L) * sigmoid(alpha * min(g, L)) * (clamp(u, -L, L) + 1).
+@pytest.mark.parametrize("gate_up,activation,limit", [
+    ("interleaved", "swiglu", 7.0),
+    ("halves", "swiglu_clamped", 0.1),        # a small limit clamps most gate and up values
+    ("interleaved", "swiglu_clamped", 0.1),
+    ("interleaved", "swiglu_clamped", 7.0),
+])
+def test_layer_variants_brute_force(golden_dir, gate_up, activation, limit):
+    table = e2m1_table(golden_dir)
+    T, H, E, k, I = 4, 64, 3, 2, 64
+    lg = syn.make_logits(T, E, "normal", seed=8).numpy()
+    hidden = bf16_bits_np(syn.make_hidden(T, H, seed=8))
+    w13, w13_sf, w2, w2_sf = rand_weights(E, H, I, seed=8)
+    w13_sf = (w13_sf.astype(np.int32) + 4).astype(np.uint8)    # x16: gate / up values of order 1, so L = 0.1 bites
+    ids, w = O.route(lg, k)
+    kw = dict(gate_up=gate_up, activation=activation, alpha=1.702, limit=limit)
+    res = O.moe_forward(hidden, ids, w, w13, w13_sf, w2, w2_sf, want=("out_f64", "a2"), **kw)
+    want, want_a2 = dense_layer(hidden, ids, w, w13, w13_sf, w2, w2_sf, table, **kw)
+    np.testing.assert_array_equal(res["a2"], want_a2)
+    np.testing.assert_allclose(res["out_f64"], want, rtol=1e-10, atol=1e-12)
+    # the variant is a different layer from the default one
+    base = O.moe_forward(hidden, ids, w, w13, w13_sf, w2, w2_sf, want=("out_f64",))["out_f64"]
+    assert not np.allclose(base, res["out_f64"])
+
+
+@pytest.mark.parametrize("activation", ["swiglu", "swiglu_clamped"])
+def test_interleaved_rows_equal_halves_layout(activation):
+    """Interleaving the rows of a gate | up w13 (row 2i <- gate i, row 2i+1 <- up i) and reading it
+    as interleaved gives exactly the halves-layout result."""
+    hidden, ids, w, w13, w13_sf, w2, w2_sf = _small_case(I=64)
+    I = w13.shape[1] // 2
+    order = np.empty(2 * I, np.int64)
+    order[0::2] = np.arange(I)
+    order[1::2] = I + np.arange(I)
+    kw = dict(activation=activation, alpha=1.702, limit=0.5)
+    a = O.moe_forward(hidden, ids, w, w13, w13_sf, w2, w2_sf, want=("out", "a2"), gate_up="halves", **kw)
+    b = O.moe_forward(hidden, ids, w, np.ascontiguousarray(w13[:, order]), np.ascontiguousarray(w13_sf[:, order]),
+                      w2, w2_sf, want=("out", "a2"), gate_up="interleaved", **kw)
+    np.testing.assert_array_equal(a["out"], b["out"])
+    np.testing.assert_array_equal(a["a2"], b["a2"])
+    # reading the halves layout as interleaved is a different (wrong) layer
+    c = O.moe_forward(hidden, ids, w, w13, w13_sf, w2, w2_sf, want=("out",), gate_up="interleaved", **kw)
+    assert not np.array_equal(a["out"], c["out"])
+
+
+def test_clamped_swiglu_one_hot_closed_form():
+    """E = k = T = 1, H = 64, I = 32, interleaved one-hot w13 rows (row 2n gate, 2n+1 up), limit 1 so that
+    gate values above 1 and up values beyond +-1 are clamped; h from the closed form in numpy."""
+    H, I, L, alpha = 64, 32, 1.0, 1.702
+    vals = [(i % 7 - 3) * 0.25 for i in range(H)]
+    x = torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16).reshape(1, H)
+    fp4_code = {1.0: 2, 1.5: 3, -2.0: 12, 0.5: 1, 3.0: 5, -1.0: 10, 4.0: 6, -3.0: 13}
+    cs = [1.0, 1.5, -2.0, 0.5, 3.0, -1.0, 4.0, -3.0]
+    g_col = [(3 * n + 1) % H for n in range(I)]
+    u_col = [(5 * n + 2) % H for n in range(I)]
+    r_col = [(7 * m + 3) % I for m in range(H)]
+    c_g = [cs[n % 8] for n in range(I)]
+    c_u = [cs[(n + 3) % 8] for n in range(I)]
+    d = [cs[(m + 4) % 6] for m in range(H)]
+    nib13 = np.zeros((1, 2 * I, H), np.uint8)
+    for n in range(I):
+        nib13[0, 2 * n, g_col[n]] = fp4_code[c_g[n]]
+        nib13[0, 2 * n + 1, u_col[n]] = fp4_code[c_u[n]]
+    nib2 = np.zeros((1, H, I), np.uint8)
+    for m in range(H):
+        nib2[0, m, r_col[m]] = fp4_code[d[m]]
+    pack = lambda nib: (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
+    w13, w2 = pack(nib13), pack(nib2)
+    w13_sf = np.full((1, 2 * I, H // 32), 127, np.uint8)
+    w2_sf = np.full((1, H, I // 32), 127, np.uint8)
+    res = O.moe_forward(bf16_bits_np(x), np.zeros((1, 1), np.int32), np.ones((1, 1), np.float32), w13, w13_sf, w2,
+                        w2_sf, want=("out_f64", "a2"), gate_up="interleaved", activation="swiglu_clamped",
+                        alpha=alpha, limit=L)
+    gate = np.array([c_g[n] * vals[g_col[n]] for n in range(I)])
+    up = np.array([c_u[n] * vals[u_col[n]] for n in range(I)])
+    assert (gate > L).any() and (up > L).any() and (up < -L).any() and (gate < -L).any()
+    gc = np.minimum(gate, L)
+    uc = np.clip(up, -L, L)
+    h = gc / (1.0 + np.exp(-alpha * gc)) * (uc + 1.0)
+    codes, sc = mxfp8_ref(h.reshape(1, I))
+    a2 = mx_dequant_e4m3(codes, sc)[0]
+    y = np.array([d[m] * a2[r_col[m]] for m in range(H)])
+    zsign = lambda c: np.where(c == 0x80, 0, c)
+    np.testing.assert_array_equal(zsign(res["a2"][0, 0]), zsign(codes[0]))
+    np.testing.assert_array_equal(res["out_f64"][0], y)
