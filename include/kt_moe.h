@@ -187,6 +187,49 @@ kt_status kt_mxfp4_moe_forward(const uint16_t* hidden, int T, int H,
                                uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Options of the gated FC1 (kt_mxfp4_moe_forward_ex).
+ *
+ * "Kimi-K3 SM120 FlashInfer MXFP4 MoE" (Phase 0 audit conclusions, item 4)
+ * notes that the SM120 MXFP4 path it audits keeps the weight layout and the
+ * parameters of GPT-OSS's SwiGLU.  Those are read as the published GPT-OSS
+ * definition:
+ *   gate_up_layout  KT_GATE_UP_HALVES:      w13 rows [0, I) gate, [I, 2I) up
+ *                   KT_GATE_UP_INTERLEAVED: w13 row 2i is gate i, row 2i+1 up i
+ *                   (w13_sf rows follow the same order)
+ *   activation      KT_ACT_SWIGLU:          h = silu(g) * u
+ *                   KT_ACT_SWIGLU_CLAMPED:  g' = min(g, limit),
+ *                                           u' = min(max(u, -limit), limit),
+ *                                           h = g' * sigmoid(alpha * g') * (u' + 1)
+ *   alpha, limit    parameters of KT_ACT_SWIGLU_CLAMPED (GPT-OSS: 1.702, 7.0);
+ *                   both finite, limit > 0; ignored by KT_ACT_SWIGLU.
+ * The two choices are independent.  A NULL options pointer means
+ * {KT_GATE_UP_HALVES, KT_ACT_SWIGLU}, which is what kt_mxfp4_moe_forward does.
+ */
+#define KT_GATE_UP_HALVES 0
+#define KT_GATE_UP_INTERLEAVED 1
+#define KT_ACT_SWIGLU 0
+#define KT_ACT_SWIGLU_CLAMPED 1
+typedef struct kt_moe_options {
+    int gate_up_layout;
+    int activation;
+    float alpha;
+    float limit;
+} kt_moe_options;
+
+/*
+ * kt_mxfp4_moe_forward with the gated-FC1 options above (opts is a HOST
+ * pointer, read during the call; NULL = defaults).  Arguments, limits,
+ * ownership and errors as kt_mxfp4_moe_forward, plus KT_ERR_INVALID_ARG for
+ * an unknown layout or activation or an invalid alpha / limit.
+ */
+kt_status kt_mxfp4_moe_forward_ex(const uint16_t* hidden, int T, int H,
+                                  const int32_t* topk_ids, const float* topk_w, int k,
+                                  const uint8_t* w13, const uint8_t* w13_sf,
+                                  const uint8_t* w2, const uint8_t* w2_sf, int E, int I,
+                                  uint16_t* out, void* ws, size_t ws_bytes,
+                                  const kt_moe_options* opts, void* stream);
+
+/*
  * Byte offsets of the forward's intermediates inside its workspace, so that
  * tests and tools can read them after a call (all relative to ws):
  *   err            i32 device error word

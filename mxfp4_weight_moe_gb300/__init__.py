@@ -49,6 +49,14 @@ class WsLayout(ctypes.Structure):
                  "y", "total")]
 
 
+class MoeOptions(ctypes.Structure):
+    _fields_ = [("gate_up_layout", ctypes.c_int), ("activation", ctypes.c_int), ("alpha", ctypes.c_float),
+                ("limit", ctypes.c_float)]
+
+
+GATE_UP_LAYOUTS = ("halves", "interleaved")
+ACTIVATIONS = ("swiglu", "swiglu_clamped")
+
 _VP, _SZ, _I = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
 
 _SIGNATURES = {
@@ -58,6 +66,8 @@ _SIGNATURES = {
     "kt_moe_route_permute": ([_VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], _I),
     "kt_moe_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
     "kt_mxfp4_moe_forward": ([_VP, _I, _I, _VP, _VP, _I, _VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _SZ, _VP], _I),
+    "kt_mxfp4_moe_forward_ex": ([_VP, _I, _I, _VP, _VP, _I, _VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _SZ,
+                                 ctypes.POINTER(MoeOptions), _VP], _I),
     "kt_moe_workspace_layout": ([_I, _I, _I, _I, _I, ctypes.POINTER(WsLayout)], _I),
     "kt_moe_read_device_error": ([_VP, ctypes.POINTER(_I), _VP], _I),
     "kt_mx_gemm_workspace_bytes": ([_I, _I, _I], _SZ),
@@ -235,8 +245,14 @@ def route_permute(logits: torch.Tensor, k: int, renormalize: bool = True, stream
 
 def forward(hidden: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, w13: torch.Tensor,
             w13_sf: torch.Tensor, w2: torch.Tensor, w2_sf: torch.Tensor, out: torch.Tensor | None = None,
-            workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """One fused MoE layer forward; returns out (bf16 [T, H])."""
+            workspace: torch.Tensor | None = None, stream=None, gate_up: str = "halves",
+            activation: str = "swiglu", alpha: float = 1.702, limit: float = 7.0) -> torch.Tensor:
+    """One fused MoE layer forward; returns out (bf16 [T, H]).
+
+    gate_up "halves" (w13 rows [0, I) gate, [I, 2I) up) or "interleaved"
+    (row 2i gate i, row 2i+1 up i); activation "swiglu" (silu(g) * u) or
+    "swiglu_clamped" (the clamped SwiGLU of GPT-OSS-format checkpoints, with
+    alpha and limit; see kt_moe_options in kt_moe.h)."""
     _need(hidden, "hidden", torch.bfloat16, 2)
     dev = hidden.device
     _need(topk_ids, "topk_ids", torch.int32, 2, dev)
@@ -255,10 +271,21 @@ def forward(hidden: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, 
     _need(out, "out", torch.bfloat16, 2, dev)
     if workspace is None:   # a caller's workspace is size-checked by the library
         workspace = torch.empty(max(workspace_bytes(T, H, I, E, k), 1), dtype=torch.uint8, device=dev)
+    if gate_up == "halves" and activation == "swiglu":
+        with _on_device(dev):
+            _check(lib().kt_mxfp4_moe_forward(_ptr(hidden), T, H, _ptr(topk_ids), _ptr(topk_w), k, _ptr(w13),
+                                              _ptr(w13_sf), _ptr(w2), _ptr(w2_sf), E, I, _ptr(out),
+                                              _ptr(workspace), workspace.numel(), _stream_ptr(stream, dev)),
+                   "kt_mxfp4_moe_forward")
+        return out
+    if gate_up not in GATE_UP_LAYOUTS or activation not in ACTIVATIONS:
+        raise ValueError(f"gate_up must be one of {GATE_UP_LAYOUTS} and activation one of {ACTIVATIONS}")
+    opts = MoeOptions(GATE_UP_LAYOUTS.index(gate_up), ACTIVATIONS.index(activation), float(alpha), float(limit))
     with _on_device(dev):
-        _check(lib().kt_mxfp4_moe_forward(_ptr(hidden), T, H, _ptr(topk_ids), _ptr(topk_w), k, _ptr(w13),
-                                          _ptr(w13_sf), _ptr(w2), _ptr(w2_sf), E, I, _ptr(out), _ptr(workspace),
-                                          workspace.numel(), _stream_ptr(stream, dev)), "kt_mxfp4_moe_forward")
+        _check(lib().kt_mxfp4_moe_forward_ex(_ptr(hidden), T, H, _ptr(topk_ids), _ptr(topk_w), k, _ptr(w13),
+                                             _ptr(w13_sf), _ptr(w2), _ptr(w2_sf), E, I, _ptr(out), _ptr(workspace),
+                                             workspace.numel(), ctypes.byref(opts), _stream_ptr(stream, dev)),
+               "kt_mxfp4_moe_forward_ex")
     return out
 
 

@@ -3,6 +3,7 @@
 // (permute -> quantise+scatter -> FC1+SwiGLU+requant -> FC2 -> combine).
 #include <cstdarg>
 #include <climits>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -188,7 +189,24 @@ kt_status kt_mxfp4_moe_forward(const uint16_t* hidden, int T, int H, const int32
                                int k, const uint8_t* w13, const uint8_t* w13_sf, const uint8_t* w2,
                                const uint8_t* w2_sf, int E, int I, uint16_t* out, void* ws, size_t ws_bytes,
                                void* stream) {
+    return kt_mxfp4_moe_forward_ex(hidden, T, H, topk_ids, topk_w, k, w13, w13_sf, w2, w2_sf, E, I, out, ws, ws_bytes,
+                                   nullptr, stream);
+}
+
+kt_status kt_mxfp4_moe_forward_ex(const uint16_t* hidden, int T, int H, const int32_t* topk_ids,
+                                  const float* topk_w, int k, const uint8_t* w13, const uint8_t* w13_sf,
+                                  const uint8_t* w2, const uint8_t* w2_sf, int E, int I, uint16_t* out, void* ws,
+                                  size_t ws_bytes, const kt_moe_options* opts, void* stream) {
     g_last_error[0] = '\0';
+    kt_moe_options o{KT_GATE_UP_HALVES, KT_ACT_SWIGLU, 1.0f, 0.0f};
+    if (opts) o = *opts;
+    if (o.gate_up_layout != KT_GATE_UP_HALVES && o.gate_up_layout != KT_GATE_UP_INTERLEAVED)
+        return fail(KT_ERR_INVALID_ARG, "gate_up_layout=%d is not a KT_GATE_UP_* value", o.gate_up_layout);
+    if (o.activation != KT_ACT_SWIGLU && o.activation != KT_ACT_SWIGLU_CLAMPED)
+        return fail(KT_ERR_INVALID_ARG, "activation=%d is not a KT_ACT_* value", o.activation);
+    if (o.activation == KT_ACT_SWIGLU_CLAMPED &&
+        !(std::isfinite(o.alpha) && std::isfinite(o.limit) && o.limit > 0.0f))
+        return fail(KT_ERR_INVALID_ARG, "clamped SwiGLU needs a finite alpha and a finite limit > 0");
     kt_status st = check_route_shape(T, E, k);
     if (st != KT_OK) return st;
     if (H <= 0 || I <= 0) return fail(KT_ERR_INVALID_ARG, "H=%d and I=%d must be positive", H, I);
@@ -254,6 +272,10 @@ kt_status kt_mxfp4_moe_forward(const uint16_t* hidden, int T, int H, const int32
     fc1.a2 = a2;
     fc1.a2_sf = a2_sf;
     fc1.err = err;
+    fc1.interleaved = o.gate_up_layout == KT_GATE_UP_INTERLEAVED ? 1 : 0;
+    fc1.activation = o.activation;
+    fc1.alpha = o.alpha;
+    fc1.limit = o.limit;
     {
         StageTimer timer(KT_STAGE_FC1, s);
         if ((st = launch_gemm(fc1, s)) != KT_OK) return st;

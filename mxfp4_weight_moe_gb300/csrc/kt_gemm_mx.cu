@@ -66,6 +66,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <unordered_map>
 
 #include "kt_common.cuh"
 #include "kt_internal.h"
@@ -152,6 +153,9 @@ struct KParams {
     int* err;
     uint64_t wait_limit_ns;
     int debug_flags;
+    int interleaved;          // FC1: w13 rows interleave gate / up (row 2i gate i, row 2i+1 up i)
+    int act;                  // FC1: 0 SwiGLU, 1 clamped SwiGLU
+    float alpha, limit;       // clamped SwiGLU parameters
 };
 
 // The routing tables a CTA decodes its work units from.  chunk_prefix is
@@ -201,14 +205,17 @@ __device__ __forceinline__ uint32_t stage_bytes(const TileInfo& ti) {
     return static_cast<uint32_t>(ti.kqs * (kQuadW + ti.nmma * 128));
 }
 
-// Coordinates of a tile's weight rows: for FC1 (view [2E][I][K] of w13)
-// (y, z) = (64 f, 2 e) selects the 64 gate rows and the 64 matching up rows;
-// otherwise (view [E * rows_w][K]) y = e * rows_w + 128 f.
+// Coordinates of a tile's weight rows: for FC1 with gate | up halves (view
+// [2E][I][K] of w13) (y, z) = (64 f, 2 e) selects the 64 gate rows and the 64
+// matching up rows; for FC1 with interleaved rows (view [E][2][I][K], the
+// [2] being row parity) (y, z) = (64 f, e); otherwise (view [E * rows_w][K])
+// y = e * rows_w + 128 f.  Either FC1 view lands the 64 gate rows and then
+// the 64 up rows in shared memory, so the MMA and epilogue are the same.
 template <int MODE>
 __device__ __forceinline__ void weight_coords(const KParams& p, const TileInfo& ti, int& y, int& z) {
     if (MODE == static_cast<int>(GemmEpilogue::SwiGLU)) {
         y = ti.f * 64;
-        z = 2 * ti.e;
+        z = p.interleaved ? ti.e : 2 * ti.e;
     } else {
         y = ti.e * p.rows_w + ti.f * 128;
         z = 0;
@@ -218,6 +225,20 @@ __device__ __forceinline__ void weight_coords(const KParams& p, const TileInfo& 
 // SiLU with the fast reciprocal-based division (the division's 2-ulp error is
 // far below the MXFP8 step the result is quantised to next).
 __device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+// The gated activation h = gate_fn(g) * up_fn(u): SwiGLU (act 0) is
+// silu(g) * u; the clamped SwiGLU of GPT-OSS-format checkpoints (act 1) is
+// g' * sigmoid(alpha g') * (u' + 1) with g' = min(g, limit) and
+// u' = clamp(u, -limit, limit).
+__device__ __forceinline__ float gate_fn(float g, int act, float alpha, float limit) {
+    if (act == 0) return silu(g);
+    const float gc = fminf(g, limit);
+    return __fdividef(gc, 1.0f + __expf(-alpha * gc));
+}
+__device__ __forceinline__ float up_fn(float u, int act, float limit) {
+    if (act == 0) return u;
+    return fminf(fmaxf(u, -limit), limit) + 1.0f;
+}
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -257,6 +278,24 @@ __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 int z, int w, int v, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z,
+                                            int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+        "[%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
         : "memory");
 }
 
@@ -302,17 +341,33 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x
                  : "memory");
 }
 
-// Load (or prefetch) a box of the weight-scale / weight-prefetch maps: 3-D for FC1, 2-D otherwise.
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int x, int y, int z, int w) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
+// Load (or prefetch) a box of the weight-scale / weight-prefetch maps: for
+// FC1 3-D (gate | up halves, z = 2e) or 4-D (interleaved rows, parity 0,
+// expert z); 2-D otherwise.
 template <int MODE>
 __device__ __forceinline__ void load_weight_box(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
-                                                int z) {
-    if (MODE == static_cast<int>(GemmEpilogue::SwiGLU)) tma_load_3d(dst, map, bar, x, y, z);
-    else tma_load_2d(dst, map, bar, x, y);
+                                                int z, bool inter) {
+    if (MODE == static_cast<int>(GemmEpilogue::SwiGLU)) {
+        if (inter) tma_load_4d(dst, map, bar, x, y, 0, z);
+        else tma_load_3d(dst, map, bar, x, y, z);
+    } else {
+        tma_load_2d(dst, map, bar, x, y);
+    }
 }
 template <int MODE>
-__device__ __forceinline__ void prefetch_weight_box(const CUtensorMap* map, int x, int y, int z) {
-    if (MODE == static_cast<int>(GemmEpilogue::SwiGLU)) tma_prefetch_l2_3d(map, x, y, z);
-    else tma_prefetch_l2_2d(map, x, y);
+__device__ __forceinline__ void prefetch_weight_box(const CUtensorMap* map, int x, int y, int z, bool inter) {
+    if (MODE == static_cast<int>(GemmEpilogue::SwiGLU)) {
+        if (inter) tma_prefetch_l2_4d(map, x, y, 0, z);
+        else tma_prefetch_l2_3d(map, x, y, z);
+    } else {
+        tma_prefetch_l2_2d(map, x, y);
+    }
 }
 
 // K-major, 128-byte-swizzled operand descriptor with `sbo` bytes between
@@ -521,7 +576,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const bool weights = warp == 0;
             bool ok = true;
-            const uint64_t pol_w = l2_policy_evict_first();
+            // weight tiles are read once per token chunk of their expert, by adjacent work units that run
+            // at about the same time: normal priority keeps them in L2 between those reads (evict-first
+            // measured 1-2 % slower on device memory and made host-resident weights cross the host link
+            // once per chunk)
+            const uint64_t pol_w = l2_policy_evict_normal();
             const uint64_t pol_a = l2_policy_evict_last();
             RingProducer rp;
             long long gi = 0;
@@ -550,7 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (weights) {
                         mbar_arrive_expect_tx(full_bar(slot), kQuadWTx * ti.kqs);
                         const CUtensorMap* wm = &maps.w[ti.kqs - 1];
-                        if (MODE == static_cast<int>(GemmEpilogue::SwiGLU))
+                        if (MODE == static_cast<int>(GemmEpilogue::SwiGLU) && p.interleaved)
+                            tma_load_5d_hint(dst, wm, full_bar(slot), 0, wy, 0, wz, kq0, pol_w);
+                        else if (MODE == static_cast<int>(GemmEpilogue::SwiGLU))
                             tma_load_4d_hint(dst, wm, full_bar(slot), 0, wy, wz, kq0, pol_w);
                         else
                             tma_load_3d_hint(dst, wm, full_bar(slot), 0, wy, kq0, pol_w);
@@ -595,12 +656,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t dst = smem_u32(stg + buf * kStgBytes);
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(stg_bar(buf), stg_tx);
-                if (p.sfa_tma) load_weight_box<MODE>(dst, &maps.wsf, stg_bar(buf), c.g * 16, c.wy, c.wz);
+                if (p.sfa_tma)
+                    load_weight_box<MODE>(dst, &maps.wsf, stg_bar(buf), c.g * 16, c.wy, c.wz, p.interleaved != 0);
                 tma_load_2d(dst + kStgSFA, &maps.asf, stg_bar(buf), c.ti.r_al, c.g * kGroup);
             }
         };
         auto prefetch_group = [&](const GroupCursor<MODE>& c) {
-            if (lane == 0 && c.valid) prefetch_weight_box<MODE>(&maps.wpf, c.g * (kGroup * 128 / 2), c.wy, c.wz);
+            if (lane == 0 && c.valid)
+                prefetch_weight_box<MODE>(&maps.wpf, c.g * (kGroup * 128 / 2), c.wy, c.wz, p.interleaved != 0);
         };
         for (int i = 0; i < kPrefetchGroups; ++i) {   // this warp's next groups
             prefetch_group(pf);
@@ -651,7 +714,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 4; ++i) {
                         const int r = lane + 32 * i;
                         size_t grow;
-                        if (MODE == static_cast<int>(GemmEpilogue::SwiGLU))
+                        if (MODE == static_cast<int>(GemmEpilogue::SwiGLU) && p.interleaved)
+                            grow = static_cast<size_t>(ti.e) * p.rows_w + 2 * (ti.f * 64 + (r & 63)) + (r < 64 ? 0 : 1);
+                        else if (MODE == static_cast<int>(GemmEpilogue::SwiGLU))
                             grow = static_cast<size_t>(ti.e) * p.rows_w + (r < 64 ? 0 : p.I) + ti.f * 64 + (r & 63);
                         else
                             grow = static_cast<size_t>(ti.e) * p.rows_w + ti.f * 128 + r;
@@ -747,13 +812,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // below 256 KB of shared memory)
                             const uint64_t dA = sdesc_sw128_sbo(sA, 1024);
                             const uint64_t dB = sdesc_sw128_sbo(sB, tok_sbo);
-                            const uint32_t acc0 = (kq0 + q) != 0 ? 1u : 0u;
+                            const bool first_quad = (kq0 + q) == 0;
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 const uint32_t idesc =
                                     idesc0 | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
-                                tc_mma_mxf8f6f4(d_tmem, dA + static_cast<uint64_t>(2 * j), dB + static_cast<uint64_t>(2 * j),
-                                                idesc, t_sfa, t_sfb, j != 0 ? 1u : acc0);
+                                const bool fresh = first_quad && j == 0;
+                                tc_mma_mxf8f6f4(d_tmem, dA + static_cast<uint64_t>(2 * j),
+                                                dB + static_cast<uint64_t>(2 * j), idesc, t_sfa, t_sfb, fresh ? 0u : 1u);
                             }
                         }
                         if (group_end) tc_commit(sf_empty(sb));
@@ -853,12 +919,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool gate = q < 2;
                     float* X = reinterpret_cast<float*>(epi) + pair * 512;          // silu(gate), columns 16-31
                     float* Y = reinterpret_cast<float*>(epi) + 1024 + pair * 512;   // up, columns 0-15
+                    const int act = p.act;
+                    const float alpha = p.alpha, limit = p.limit;
                     if (gate) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) X[j * 32 + lane] = silu(__uint_as_float(v[16 + j]));
+                        for (int j = 0; j < 16; ++j)
+                            X[j * 32 + lane] = gate_fn(__uint_as_float(v[16 + j]), act, alpha, limit);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) Y[j * 32 + lane] = __uint_as_float(v[j]);
+                        for (int j = 0; j < 16; ++j) Y[j * 32 + lane] = up_fn(__uint_as_float(v[j]), act, limit);
                     }
                     named_bar_sync(1, 128);
                     uint8_t* my_bt = epi + 8192 + q * 512;   // [16 columns][32 features]
@@ -866,8 +935,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float hv[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        hv[j] = gate ? silu(__uint_as_float(v[j])) * Y[j * 32 + lane]
-                                     : X[j * 32 + lane] * __uint_as_float(v[16 + j]);
+                        hv[j] = gate ? gate_fn(__uint_as_float(v[j]), act, alpha, limit) * Y[j * 32 + lane]
+                                     : X[j * 32 + lane] * up_fn(__uint_as_float(v[16 + j]), act, limit);
                     uint32_t am[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
@@ -935,13 +1004,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// tiled map of rank 2-4 (dims/box innermost first; strides in bytes for dims 1..rank-1)
+// tiled map of rank 2-5 (dims/box innermost first; strides in bytes for dims 1..rank-1)
+constexpr int kMaxMapRank = 5;
 static bool encode(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank, const uint64_t* dims,
                    const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw) {
     auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t d[4], st[3];
-    cuuint32_t b[4], es[4] = {1, 1, 1, 1};
+    if (!fn || rank < 1 || rank > kMaxMapRank) return false;
+    cuuint64_t d[kMaxMapRank], st[kMaxMapRank - 1];
+    cuuint32_t b[kMaxMapRank], es[kMaxMapRank] = {1, 1, 1, 1, 1};
     for (int i = 0; i < rank; ++i) {
         d[i] = dims[i];
         b[i] = box[i];
@@ -1036,17 +1106,25 @@ static cudaError_t launch_mode(const GemmMaps& maps, KParams kp, int max_cluster
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-kt_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
-    if (a.S <= 0) return KT_OK;
-    alignas(64) GemmMaps maps;
+// Every tensor map of one launch.  The maps are a pure function of the
+// pointers and sizes they describe, so they are cached (MapCache below).
+static bool encode_maps(const GemmArgs& a, GemmMaps& maps) {
     const bool fc1 = a.mode == GemmEpilogue::SwiGLU;
     const uint64_t K = static_cast<uint64_t>(a.K);
     const uint64_t wrows = static_cast<uint64_t>(a.E) * a.rows_w;
     const int S4 = sf_rows(a.S);
     const bool sfa_tma = (a.K % 512) == 0;
     bool ok = true;
+    const bool inter = fc1 && a.interleaved;
     for (int kq = 1; kq <= 2; ++kq) {
-        if (fc1) {
+        if (inter) {
+            // interleaved w13 viewed as [K/128 quad][E][2 parity][I][128]: row 2i + parity of expert e
+            const uint64_t dw[5] = {128, static_cast<uint64_t>(a.I), 2, static_cast<uint64_t>(a.E), K / 128};
+            const uint64_t sw[4] = {K, K / 2, static_cast<uint64_t>(a.I) * K, 64};
+            const uint32_t bw[5] = {128, 64, 2, 1, static_cast<uint32_t>(kq)};
+            ok = ok && encode(&maps.w[kq - 1], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.w, 5, dw, sw, bw,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+        } else if (fc1) {
             // w13 viewed as [K/128 quad][2E][I][128]: (z = 2e + gate/up, y = row within the half)
             const uint64_t dw[4] = {128, static_cast<uint64_t>(a.I), 2ull * a.E, K / 128};
             const uint64_t sw[3] = {K / 2, static_cast<uint64_t>(a.I) * (K / 2), 64};
@@ -1072,7 +1150,19 @@ kt_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
                               CU_TENSOR_MAP_SWIZZLE_128B);
         }
     }
-    if (fc1) {
+    if (inter) {
+        const uint64_t dp[4] = {K / 2, static_cast<uint64_t>(a.I), 2, static_cast<uint64_t>(a.E)};
+        const uint64_t sp[3] = {K, K / 2, static_cast<uint64_t>(a.I) * K};
+        const uint32_t bp[4] = {static_cast<uint32_t>(kGroup * 128 / 2), 64, 2, 1};
+        ok = ok && encode(&maps.wpf, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w, 4, dp, sp, bp, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (sfa_tma) {
+            const uint64_t ds[4] = {K / 32, static_cast<uint64_t>(a.I), 2, static_cast<uint64_t>(a.E)};
+            const uint64_t ss[3] = {K / 16, K / 32, static_cast<uint64_t>(a.I) * (K / 16)};
+            const uint32_t bs[4] = {16, 64, 2, 1};
+            ok = ok && encode(&maps.wsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_sf, 4, ds, ss, bs,
+                              CU_TENSOR_MAP_SWIZZLE_NONE);
+        }
+    } else if (fc1) {
         const uint64_t dp[3] = {K / 2, static_cast<uint64_t>(a.I), 2ull * a.E};
         const uint64_t sp[2] = {K / 2, static_cast<uint64_t>(a.I) * (K / 2)};
         const uint32_t bp[3] = {static_cast<uint32_t>(kGroup * 128 / 2), 64, 2};
@@ -1105,7 +1195,86 @@ kt_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
         ok = ok && encode(&maps.asf, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.act_sf, 2, da, sa, ba,
                           CU_TENSOR_MAP_SWIZZLE_NONE);
     }
-    if (!ok) return report(KT_ERR_CUDA, "tensor map encoding failed");
+    return ok;
+}
+
+// Tensor maps cached per (device, epilogue, layout, pointers, sizes): a
+// decode-sized forward would otherwise spend much of its host time encoding
+// the same ~53 maps per GEMM launch on every call.  The key holds everything
+// a map depends on (a map is bytes: the addresses and sizes it describes,
+// valid in any context), so an entry never goes stale; re-allocated memory
+// at the same address with the same sizes maps to the same bytes.  Bounded:
+// the table is cleared when it reaches kMapCacheEntries.
+struct MapKey {
+    int dev, mode, interleaved, K, E, rows_w, I, S;
+    const void *w, *w_sf, *act, *act_sf;
+    bool operator==(const MapKey& o) const {
+        return dev == o.dev && mode == o.mode && interleaved == o.interleaved && K == o.K && E == o.E &&
+               rows_w == o.rows_w && I == o.I && S == o.S && w == o.w && w_sf == o.w_sf && act == o.act &&
+               act_sf == o.act_sf;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+        uint64_t h = 1469598103934665603ull;
+        auto mix = [&h](uint64_t v) {
+            h ^= v;
+            h *= 1099511628211ull;
+        };
+        mix(static_cast<uint64_t>(k.dev));
+        mix(static_cast<uint64_t>(k.mode) | (static_cast<uint64_t>(k.interleaved) << 8));
+        mix(static_cast<uint64_t>(k.K));
+        mix(static_cast<uint64_t>(k.E));
+        mix(static_cast<uint64_t>(k.rows_w));
+        mix(static_cast<uint64_t>(k.I));
+        mix(static_cast<uint64_t>(k.S));
+        mix(reinterpret_cast<uintptr_t>(k.w));
+        mix(reinterpret_cast<uintptr_t>(k.w_sf));
+        mix(reinterpret_cast<uintptr_t>(k.act));
+        mix(reinterpret_cast<uintptr_t>(k.act_sf));
+        return static_cast<size_t>(h);
+    }
+};
+constexpr size_t kMapCacheEntries = 256;
+static std::mutex g_map_mu;
+static std::unordered_map<MapKey, GemmMaps, MapKeyHash>& map_cache() {
+    static std::unordered_map<MapKey, GemmMaps, MapKeyHash> m;
+    return m;
+}
+
+#ifndef KT_MAP_CACHE
+#define KT_MAP_CACHE 1
+#endif
+
+static bool get_maps(const GemmArgs& a, GemmMaps& maps) {
+    if (!KT_MAP_CACHE) return encode_maps(a, maps);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const MapKey key{dev, static_cast<int>(a.mode), a.mode == GemmEpilogue::SwiGLU ? a.interleaved : 0, a.K, a.E,
+                     a.rows_w, a.I, a.S, a.w, a.w_sf, a.act, a.act_sf};
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        auto it = map_cache().find(key);
+        if (it != map_cache().end()) {
+            maps = it->second;
+            return true;
+        }
+    }
+    if (!encode_maps(a, maps)) return false;
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (map_cache().size() >= kMapCacheEntries) map_cache().clear();
+    map_cache().emplace(key, maps);
+    return true;
+}
+
+kt_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
+    if (a.S <= 0) return KT_OK;
+    alignas(64) GemmMaps maps;
+    const bool fc1 = a.mode == GemmEpilogue::SwiGLU;
+    const bool inter = fc1 && a.interleaved;
+    const int S4 = sf_rows(a.S);
+    const bool sfa_tma = (a.K % 512) == 0;
+    if (!get_maps(a, maps)) return report(KT_ERR_CUDA, "tensor map encoding failed");
     KParams kp{};
     kp.expert_offsets = a.expert_offsets;
     kp.chunk_prefix = a.chunk_prefix;
@@ -1129,6 +1298,10 @@ kt_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
     const DebugSettings dbg = debug_settings();
     kp.wait_limit_ns = dbg.wait_limit_ns;
     kp.debug_flags = dbg.flags;
+    kp.interleaved = inter ? 1 : 0;
+    kp.act = fc1 ? a.activation : 0;
+    kp.alpha = a.alpha;
+    kp.limit = a.limit;
     const int max_cluster = kGemmMaxCluster;
     cudaError_t e;
     switch (a.mode) {

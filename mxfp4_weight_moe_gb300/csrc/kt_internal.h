@@ -114,6 +114,10 @@ struct GemmArgs {
     // Raw output: f32 [S, rows_w]
     float* raw_out;
     int* err;
+    // SwiGLU: w13 gate/up row layout and gated activation (kt_moe_options)
+    int interleaved = 0;
+    int activation = 0;
+    float alpha = 1.0f, limit = 0.0f;
 };
 
 // Test-hook settings (kt_moe_debug_configure), read at each GEMM launch.

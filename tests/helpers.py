@@ -59,13 +59,14 @@ def sample_tokens(ids: np.ndarray, n: int, seed: int = 0) -> np.ndarray:
 
 
 def oracle_subset(hidden_bits, ids, w, w13, w13_sf, w2, w2_sf, tokens, want=("out", "a2", "a2_sf"),
-                  batch_bytes=6e9):
+                  batch_bytes=6e9, **opts):
     """Oracle on a token subset using only the experts those tokens touch.
 
     w13 ... may be torch CUDA tensors; only the touched experts are copied to
     the host (ids are remapped to the compact expert list).  Tokens go in
     batches whose touched experts hold at most about batch_bytes, so that a
-    sample of the 36.7 GB Kimi-K3-shaped layer never copies it all."""
+    sample of the 36.7 GB Kimi-K3-shaped layer never copies it all.  opts
+    (gate_up, activation, alpha, limit) go to the oracle's forward."""
     E = w13.shape[0]
     per_expert = sum(t[0].numel() * t.element_size() for t in (w13, w13_sf, w2, w2_sf))
     tokens = np.asarray(tokens, np.int32)
@@ -82,7 +83,7 @@ def oracle_subset(hidden_bits, ids, w, w13, w13_sf, w2, w2_sf, tokens, want=("ou
         idx = torch.from_numpy(used).to(w13.device)
         W = [t.index_select(0, idx).cpu().numpy() for t in (w13, w13_sf, w2, w2_sf)]
         rid = np.where(ok, remap[np.clip(sub_ids, 0, E)], -1)
-        parts.append(O.moe_forward(hidden_bits[tk], rid.astype(np.int32), w[tk], *W, want=want))
+        parts.append(O.moe_forward(hidden_bits[tk], rid.astype(np.int32), w[tk], *W, want=want, **opts))
         del W
     return {key: np.concatenate([p[key] for p in parts], axis=0) for key in parts[0]}
 
