@@ -311,15 +311,26 @@ def run_ours(args, cfg, full: bool = True):
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(h=hidden, lg=logits):
-        ids, w, *_ = kt.route_permute(lg, k, out=route_out, workspace=ws_route, stream=stream)
-        kt.forward(h, ids, w, *W, out=out, workspace=ws, stream=stream)
+    # decode-sized batches run as ONE launch (routing, permutation and the layer forward)
+    use_decode = args.path == "decode" or (args.path == "auto" and T * k <= kt.DECODE_MAX_SLOTS)
+
+    def step(h=hidden, lg=logits, o=out, s=stream):
+        if use_decode:
+            kt.decode(lg, h, k, *W, out=o, topk=route_out[:2], workspace=ws, stream=s)
+        else:
+            ids, w, *_ = kt.route_permute(lg, k, out=route_out, workspace=ws_route, stream=s)
+            kt.forward(h, ids, w, *W, out=o, workspace=ws, stream=s)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     assert kt.read_device_error(ws) == 0, "device error word set during warm-up"
-    counts = (route_out[2][1:] - route_out[2][:-1]).cpu()
+    if use_decode:   # the offsets live in the workspace on this path
+        lay = kt.workspace_layout(T, H, I, E, k)
+        offs = ws[lay["expert_offsets"]:lay["expert_offsets"] + 4 * (E + 1)].view(torch.int32)
+        counts = (offs[1:] - offs[:-1]).cpu()
+    else:
+        counts = (route_out[2][1:] - route_out[2][:-1]).cpu()
     touched = int((counts > 0).sum())
 
     # ---- timed region: device-resident inputs
@@ -348,6 +359,8 @@ def run_ours(args, cfg, full: bool = True):
         step()
     prof = kt.profile_read()
     kt.profile_enable(False)
+    if use_decode:   # one kernel for the whole layer: its time is the step's
+        prof_fc1 = (elapsed_ms, args.steps)
     ms_per_step = elapsed_ms / args.steps
     value = T / (ms_per_step / 1e3)
 
@@ -374,8 +387,7 @@ def run_ours(args, cfg, full: bool = True):
         ev_in[b].record(s_in)
         stream.wait_event(ev_in[b])
         stream.wait_event(ev_out[b])           # step i-2's result left this output buffer
-        ids, w, *_ = kt.route_permute(lg_dev[b], k, out=route_out, workspace=ws_route, stream=stream)
-        kt.forward(h_dev[b], ids, w, *W, out=out_dev[b], workspace=ws, stream=stream)
+        step(h_dev[b], lg_dev[b], out_dev[b])
         ev_done[b].record(stream)
         s_out.wait_event(ev_done[b])
         with torch.cuda.stream(s_out):
@@ -392,8 +404,7 @@ def run_ours(args, cfg, full: bool = True):
             b = i % 2
             h_dev[b].copy_(h_host, non_blocking=True)
             lg_dev[b].copy_(lg_host, non_blocking=True)
-            ids, w, *_ = kt.route_permute(lg_dev[b], k, out=route_out, workspace=ws_route, stream=stream)
-            kt.forward(h_dev[b], ids, w, *W, out=out_dev[b], workspace=ws, stream=stream)
+            step(h_dev[b], lg_dev[b], out_dev[b])
             out_host[b].copy_(out_dev[b], non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 50))
@@ -418,8 +429,7 @@ def run_ours(args, cfg, full: bool = True):
         gstream.wait_stream(stream)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=gstream):
-            ids_g, w_g, *_ = kt.route_permute(logits, k, out=route_out, workspace=ws_route, stream=gstream)
-            kt.forward(hidden, ids_g, w_g, *W, out=out, workspace=ws, stream=gstream)
+            step(s=gstream)
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize(dev)
@@ -441,7 +451,9 @@ def run_ours(args, cfg, full: bool = True):
     fc2_ms = prof["fc2"][0] / max(1, prof["fc2"][1])
     hbm = float(peaks["hbm_gbs"])
     mx_tflops = float(peaks["bf16_tflops"]) * FP8_OVER_BF16
-    fc1_gbs = work["fc1_bytes"] / (fc1_ms / 1e3) / 1e9
+    # the decode path's one kernel moves the whole layer's bytes
+    dom_bytes = work["layer_bytes"] if use_decode else work["fc1_bytes"]
+    fc1_gbs = dom_bytes / (fc1_ms / 1e3) / 1e9
     t_roof_ms = 1e3 * max(work["layer_flops"] / (mx_tflops * 1e12), work["layer_bytes"] / (hbm * 1e9))
     res = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
@@ -456,9 +468,13 @@ def run_ours(args, cfg, full: bool = True):
         "graph": graph,
         "clocks": clocks,
         "roofline": {"bound": "hbm", "achieved": fc1_gbs, "peak": hbm, "unit": "GB/s", "frac": fc1_gbs / hbm,
-                     "traffic": fc1_traffic(cfg.name), "kernel": "mx_gemm_kernel<SwiGLU> (FC1)",
+                     "traffic": None if use_decode else fc1_traffic(cfg.name),
+                     "kernel": "moe_decode_kernel (whole layer, one launch)" if use_decode
+                     else "mx_gemm_kernel<SwiGLU> (FC1)",
                      "peak_source": f"{peak_src} hbm_gbs",
-                     "algorithmic_bytes_per_launch": work["fc1_bytes"], "avg_launch_ms": fc1_ms},
+                     "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": fc1_ms},
+        "path": "decode: one launch (route, permute, quantise, FC1, FC2, combine)" if use_decode
+        else "route_permute + forward (7 launches)",
         "layer_roofline": {"t_roof_ms": t_roof_ms, "frac": t_roof_ms / ms_per_step,
                            "bytes": work["layer_bytes"], "flops": work["layer_flops"],
                            "hbm_gbs": hbm, "mx_tflops": mx_tflops,
@@ -479,7 +495,7 @@ def run_ours(args, cfg, full: bool = True):
 
 def secondary_summary(res: dict) -> dict:
     keep = ("value", "unit", "ms_per_step", "config", "e2e", "gpu_launches", "graph", "roofline", "layer_roofline",
-            "stage_ms", "fc2_gbs", "clocks")
+            "stage_ms", "fc2_gbs", "clocks", "path")
     return {k: res[k] for k in keep if k in res}
 
 
@@ -596,6 +612,8 @@ def main():
     ap.add_argument("--secondary", default="dsv4", help="a second workload measured after the first and nested "
                                                           "under 'secondary' ('none' to skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=("auto", "decode", "multi"), default="auto",
+                    help="auto: the single-launch decode kernel when T * top_k <= 2048, else route_permute + forward")
     ap.add_argument("--ref-budget-s", type=float, default=150.0)
     ap.add_argument("--layer-stores", type=int, default=4,
                     help="layerwise workload: distinct pinned host layer stores, cycled over the layers")

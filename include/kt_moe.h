@@ -77,6 +77,7 @@ typedef int kt_status;
 #define KT_DEVERR_TIMEOUT_LOAD 0x2    /* GEMM producer wait expired */
 #define KT_DEVERR_TIMEOUT_MMA 0x4     /* GEMM MMA-issuer wait expired */
 #define KT_DEVERR_TIMEOUT_EPI 0x8     /* GEMM epilogue wait expired */
+#define KT_DEVERR_TIMEOUT_GRID 0x10   /* decode kernel: a grid-wide barrier wait expired */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* kt_status_string(kt_status status);
@@ -228,6 +229,37 @@ kt_status kt_mxfp4_moe_forward_ex(const uint16_t* hidden, int T, int H,
                                   const uint8_t* w2, const uint8_t* w2_sf, int E, int I,
                                   uint16_t* out, void* ws, size_t ws_bytes,
                                   const kt_moe_options* opts, void* stream);
+
+/*
+ * Single-launch decode: routing, permutation and the layer forward in ONE
+ * kernel launch, for decode-sized batches (T * k <= KT_DECODE_MAX_SLOTS).
+ * It computes exactly what kt_moe_route_permute followed by
+ * kt_mxfp4_moe_forward_ex compute (same ids, weights, permutation and
+ * kernels' arithmetic), without their seven launches: one cooperative kernel
+ * with one CTA per SM runs route -> permute -> MXFP8 quantisation -> FC1 +
+ * SwiGLU -> FC2 -> combine, with grid-wide barriers (each wait bounded by the
+ * same deadline as the GEMM barriers; an expired wait sets
+ * KT_DEVERR_TIMEOUT_GRID and the kernel returns).
+ * ("Kimi-K3 SM120 FlashInfer MXFP4 MoE", later hard gates, item 5: token
+ * counts 1/2/8/32 and CUDA Graph capture/replay.)
+ *   logits      f32 [T, E] router logits; renormalize as for
+ *               kt_moe_route_permute
+ *   hidden .. w2_sf, opts   as for kt_mxfp4_moe_forward_ex
+ *   topk_ids    i32 [T, k] out;  topk_w f32 [T, k] out (16-byte aligned)
+ *   out         bf16 [T, H] out
+ *   ws          >= kt_moe_workspace_bytes(T, H, I, E, k), 256-byte aligned,
+ *               same layout (kt_moe_workspace_layout); bytes 64-191 of its
+ *               error region hold the kernel's barrier counters
+ * Errors as kt_mxfp4_moe_forward_ex, plus KT_ERR_UNSUPPORTED_SHAPE when
+ * T * k > KT_DECODE_MAX_SLOTS.  Needs every SM free for one CTA (a
+ * cooperative launch): KT_ERR_CUDA when the device cannot co-schedule it.
+ */
+#define KT_DECODE_MAX_SLOTS 2048
+kt_status kt_mxfp4_moe_decode(const float* logits, const uint16_t* hidden, int T, int H, int E, int k, int I,
+                              int renormalize, const uint8_t* w13, const uint8_t* w13_sf,
+                              const uint8_t* w2, const uint8_t* w2_sf,
+                              int32_t* topk_ids, float* topk_w, uint16_t* out,
+                              void* ws, size_t ws_bytes, const kt_moe_options* opts, void* stream);
 
 /*
  * Byte offsets of the forward's intermediates inside its workspace, so that

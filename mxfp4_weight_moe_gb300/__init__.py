@@ -24,7 +24,7 @@ from . import build_ext
 __all__ = [
     "KTError", "lib", "route_permute", "forward", "workspace_bytes", "workspace_layout", "read_device_error",
     "grouped_gemm_f32", "Layerwise", "status_string", "check_fc_shapes", "kernel_launches", "profile_enable",
-    "profile_read", "STAGES", "route_permute_noalloc",
+    "profile_read", "STAGES", "route_permute_noalloc", "decode", "DECODE_MAX_SLOTS",
 ]
 
 KT_OK = 0
@@ -68,6 +68,8 @@ _SIGNATURES = {
     "kt_mxfp4_moe_forward": ([_VP, _I, _I, _VP, _VP, _I, _VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _SZ, _VP], _I),
     "kt_mxfp4_moe_forward_ex": ([_VP, _I, _I, _VP, _VP, _I, _VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _SZ,
                                  ctypes.POINTER(MoeOptions), _VP], _I),
+    "kt_mxfp4_moe_decode": ([_VP, _VP, _I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
+                             ctypes.POINTER(MoeOptions), _VP], _I),
     "kt_moe_workspace_layout": ([_I, _I, _I, _I, _I, ctypes.POINTER(WsLayout)], _I),
     "kt_moe_read_device_error": ([_VP, ctypes.POINTER(_I), _VP], _I),
     "kt_mx_gemm_workspace_bytes": ([_I, _I, _I], _SZ),
@@ -92,6 +94,7 @@ _SIGNATURES = {
 }
 
 KT_NOALLOC_SCRATCH_BYTES = 1 << 20
+DECODE_MAX_SLOTS = 2048   # KT_DECODE_MAX_SLOTS
 
 KT_DEBUG_WITHHOLD_STAGE = 0x1
 
@@ -287,6 +290,45 @@ def forward(hidden: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, 
                                              workspace.numel(), ctypes.byref(opts), _stream_ptr(stream, dev)),
                "kt_mxfp4_moe_forward_ex")
     return out
+
+
+def decode(logits: torch.Tensor, hidden: torch.Tensor, k: int, w13: torch.Tensor, w13_sf: torch.Tensor,
+           w2: torch.Tensor, w2_sf: torch.Tensor, renormalize: bool = True, out: torch.Tensor | None = None,
+           topk: tuple | None = None, workspace: torch.Tensor | None = None, stream=None,
+           gate_up: str = "halves", activation: str = "swiglu", alpha: float = 1.702, limit: float = 7.0):
+    """Routing + the layer forward in ONE kernel launch (T * k <= DECODE_MAX_SLOTS).
+
+    Same results as route_permute followed by forward.  Returns
+    (out bf16 [T, H], topk_ids int32 [T, k], topk_w float32 [T, k])."""
+    _need(logits, "logits", torch.float32, 2)
+    dev = logits.device
+    _need(hidden, "hidden", torch.bfloat16, 2, dev)
+    for name, t in (("w13", w13), ("w13_sf", w13_sf), ("w2", w2), ("w2_sf", w2_sf)):
+        _need(t, name, torch.uint8, 3, dev)
+    E, I, H = check_fc_shapes(w13, w2)
+    T = hidden.shape[0]
+    if hidden.shape != (T, H) or logits.shape != (T, E):
+        raise ValueError(f"hidden {tuple(hidden.shape)} / logits {tuple(logits.shape)} do not match T={T}, H={H}, "
+                         f"E={E}")
+    if w13_sf.shape != (E, 2 * I, H // 32) or w2_sf.shape != (E, H, I // 32):
+        raise ValueError("scale tensors must be [E, 2I, H/32] and [E, H, I/32]")
+    if gate_up not in GATE_UP_LAYOUTS or activation not in ACTIVATIONS:
+        raise ValueError(f"gate_up must be one of {GATE_UP_LAYOUTS} and activation one of {ACTIVATIONS}")
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, 2, dev)
+    if topk is None:
+        topk = (torch.empty(T, k, dtype=torch.int32, device=dev), torch.empty(T, k, dtype=torch.float32, device=dev))
+    ids, w = topk
+    if workspace is None:
+        workspace = torch.empty(max(workspace_bytes(T, H, I, E, k), 1), dtype=torch.uint8, device=dev)
+    opts = MoeOptions(GATE_UP_LAYOUTS.index(gate_up), ACTIVATIONS.index(activation), float(alpha), float(limit))
+    with _on_device(dev):
+        _check(lib().kt_mxfp4_moe_decode(_ptr(logits), _ptr(hidden), T, H, E, k, I, int(bool(renormalize)),
+                                         _ptr(w13), _ptr(w13_sf), _ptr(w2), _ptr(w2_sf), _ptr(ids), _ptr(w), _ptr(out),
+                                         _ptr(workspace), workspace.numel(), ctypes.byref(opts),
+                                         _stream_ptr(stream, dev)), "kt_mxfp4_moe_decode")
+    return out, ids, w
 
 
 def read_device_error(workspace: torch.Tensor, stream=None) -> int:

@@ -307,6 +307,117 @@ kt_status kt_mxfp4_moe_forward_ex(const uint16_t* hidden, int T, int H, const in
     return cuda_status(launch_combine(y, topk_ids, T, H, k, E, out, s));
 }
 
+kt_status kt_mxfp4_moe_decode(const float* logits, const uint16_t* hidden, int T, int H, int E, int k, int I,
+                              int renormalize, const uint8_t* w13, const uint8_t* w13_sf, const uint8_t* w2,
+                              const uint8_t* w2_sf, int32_t* topk_ids, float* topk_w, uint16_t* out, void* ws,
+                              size_t ws_bytes, const kt_moe_options* opts, void* stream) {
+    g_last_error[0] = '\0';
+    kt_moe_options o{KT_GATE_UP_HALVES, KT_ACT_SWIGLU, 1.0f, 0.0f};
+    if (opts) o = *opts;
+    if (o.gate_up_layout != KT_GATE_UP_HALVES && o.gate_up_layout != KT_GATE_UP_INTERLEAVED)
+        return fail(KT_ERR_INVALID_ARG, "gate_up_layout=%d is not a KT_GATE_UP_* value", o.gate_up_layout);
+    if (o.activation != KT_ACT_SWIGLU && o.activation != KT_ACT_SWIGLU_CLAMPED)
+        return fail(KT_ERR_INVALID_ARG, "activation=%d is not a KT_ACT_* value", o.activation);
+    if (o.activation == KT_ACT_SWIGLU_CLAMPED &&
+        !(std::isfinite(o.alpha) && std::isfinite(o.limit) && o.limit > 0.0f))
+        return fail(KT_ERR_INVALID_ARG, "clamped SwiGLU needs a finite alpha and a finite limit > 0");
+    kt_status st = check_route_shape(T, E, k);
+    if (st != KT_OK) return st;
+    if (H <= 0 || I <= 0) return fail(KT_ERR_INVALID_ARG, "H=%d and I=%d must be positive", H, I);
+    if (H % 128 || I % 128)
+        return fail(KT_ERR_UNSUPPORTED_SHAPE, "H=%d and I=%d must be multiples of 128", H, I);
+    if (static_cast<long long>(E) * 2 * I > INT_MAX / 2 || static_cast<long long>(E) * H > INT_MAX / 2)
+        return fail(KT_ERR_UNSUPPORTED_SHAPE, "E*2I or E*H too large");
+    if (static_cast<long long>(T) * k > KT_DECODE_MAX_SLOTS)
+        return fail(KT_ERR_UNSUPPORTED_SHAPE, "T*k=%lld slots above the decode kernel's %d",
+                    static_cast<long long>(T) * k, KT_DECODE_MAX_SLOTS);
+    if (T == 0) return KT_OK;
+    if (!logits || !hidden || !topk_ids || !topk_w || !w13 || !w13_sf || !w2 || !w2_sf || !out || !ws)
+        return fail(KT_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(logits, 4) || !aligned(hidden, 16) || !aligned(out, 16) || !aligned(topk_ids, 16) ||
+        !aligned(topk_w, 16))
+        return fail(KT_ERR_ALIGNMENT, "logits must be 4-byte and hidden, out, topk_ids, topk_w 16-byte aligned");
+    if (!aligned(w13, 32) || !aligned(w2, 32))
+        return fail(KT_ERR_ALIGNMENT, "w13 and w2 must be 32-byte aligned");
+    if (!aligned(w13_sf, 16) || !aligned(w2_sf, 16))
+        return fail(KT_ERR_ALIGNMENT, "w13_sf and w2_sf must be 16-byte aligned");
+    kt_ws_layout L;
+    ws_layout(T, H, I, E, k, &L);
+    if (!aligned(ws, 256)) return fail(KT_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (ws_bytes < L.total) return fail(KT_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, L.total);
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    int* err = reinterpret_cast<int*>(base + L.err);
+    int32_t* offsets = reinterpret_cast<int32_t*>(base + L.expert_offsets);
+    int32_t* chunk_prefix = reinterpret_cast<int32_t*>(base + L.chunk_prefix);
+    int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
+    const long long S = static_cast<long long>(T) * k;
+    // the error word and the kernel's two grid counters share the 256-byte error region
+    if ((st = cuda_status(cudaMemsetAsync(base + L.err, 0, 256, s))) != KT_OK) return st;
+
+    GemmArgs fc1{};
+    fc1.mode = GemmEpilogue::SwiGLU;
+    fc1.expert_offsets = offsets;
+    fc1.chunk_prefix = chunk_prefix;
+    fc1.E = E;
+    fc1.K = H;
+    fc1.rows_w = 2 * I;
+    fc1.I = I;
+    fc1.S = static_cast<int>(S);
+    fc1.H = H;
+    fc1.w = w13;
+    fc1.w_sf = w13_sf;
+    fc1.act = base + L.a1;
+    fc1.act_sf = base + L.a1_sf;
+    fc1.a2 = base + L.a2;
+    fc1.a2_sf = base + L.a2_sf;
+    fc1.err = err;
+    fc1.interleaved = o.gate_up_layout == KT_GATE_UP_INTERLEAVED ? 1 : 0;
+    fc1.activation = o.activation;
+    fc1.alpha = o.alpha;
+    fc1.limit = o.limit;
+    GemmArgs fc2{};
+    fc2.mode = GemmEpilogue::Combine;
+    fc2.expert_offsets = offsets;
+    fc2.chunk_prefix = chunk_prefix;
+    fc2.E = E;
+    fc2.K = I;
+    fc2.rows_w = H;
+    fc2.I = I;
+    fc2.S = static_cast<int>(S);
+    fc2.H = H;
+    fc2.w = w2;
+    fc2.w_sf = w2_sf;
+    fc2.act = base + L.a2;
+    fc2.act_sf = base + L.a2_sf;
+    fc2.y = reinterpret_cast<uint16_t*>(base + L.y);
+    fc2.perm = perm;
+    fc2.topk_w = topk_w;
+    fc2.err = err;
+    DecodeInputs in{};
+    in.logits = logits;
+    in.hidden = hidden;
+    in.T = T;
+    in.H = H;
+    in.E = E;
+    in.k = k;
+    in.renormalize = renormalize ? 1 : 0;
+    in.ids = topk_ids;
+    in.w = topk_w;
+    in.offsets = offsets;
+    in.chunk_prefix = chunk_prefix;
+    in.perm = perm;
+    in.inv_perm = reinterpret_cast<int32_t*>(base + L.inv_perm);
+    in.a1 = base + L.a1;
+    in.a1_sf = base + L.a1_sf;
+    in.y = reinterpret_cast<const uint16_t*>(base + L.y);
+    in.out = out;
+    in.grid_ctr = reinterpret_cast<unsigned*>(base + L.err + 64);
+    in.fc1_done = reinterpret_cast<unsigned*>(base + L.err + 128);
+    return launch_decode(fc1, fc2, in, s);
+}
+
 kt_status kt_moe_read_device_error(const void* ws, int* code, void* stream) {
     g_last_error[0] = '\0';
     if (!ws || !code) return fail(KT_ERR_INVALID_ARG, "null pointer argument");
@@ -316,7 +427,7 @@ kt_status kt_moe_read_device_error(const void* ws, int* code, void* stream) {
     int v = 0;
     if ((st = cuda_status(cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost))) != KT_OK) return st;
     *code = v;
-    if (v & (KT_DEVERR_TIMEOUT_LOAD | KT_DEVERR_TIMEOUT_MMA | KT_DEVERR_TIMEOUT_EPI))
+    if (v & (KT_DEVERR_TIMEOUT_LOAD | KT_DEVERR_TIMEOUT_MMA | KT_DEVERR_TIMEOUT_EPI | KT_DEVERR_TIMEOUT_GRID))
         return fail(KT_ERR_DEVICE_TIMEOUT, "device error word 0x%x", v);
     if (v & KT_DEVERR_BAD_EXPERT_ID) return fail(KT_ERR_BAD_EXPERT_ID, "device error word 0x%x", v);
     return KT_OK;

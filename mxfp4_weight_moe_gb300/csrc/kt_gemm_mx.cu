@@ -69,7 +69,9 @@
 #include <unordered_map>
 
 #include "kt_common.cuh"
+#include "kt_decode_dev.cuh"
 #include "kt_internal.h"
+#include "kt_quant_dev.cuh"
 
 namespace kt {
 
@@ -107,12 +109,13 @@ constexpr int kThreads = 288;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kTileTokens;    // accumulator buffer b at column b * kAccCols
 constexpr uint32_t kTmemSF = 2 * kAccCols;    // scale columns after both accumulators
-constexpr uint32_t kSfSlotCols = 24;          // per stage: 2 quads x (4 weight + 8 token columns)
+constexpr uint32_t kSfQuadCols = 12;          // per K quad: 4 weight + 8 token scale columns
+constexpr uint32_t kSfGroupCols = kGroup * kSfQuadCols;   // one scale group's tensor-memory buffer (two of them)
 constexpr int kPrefetchGroups = 2;            // scale-warp L2 prefetch distance, in groups
 // the largest stage always fits once every earlier stage is released
 static_assert(2 * kQuadW + kSmallN * 256 <= kRing && kQuadW + kTileTokens * 128 <= kRing, "stage ring");
 static_assert(kSmemTotal <= 232448, "shared memory budget");
-static_assert(kTmemSF + kSfSlotCols * kSlots <= kTmemCols, "tensor memory budget");
+static_assert(kTmemSF + 2 * kSfGroupCols <= kTmemCols, "tensor memory budget");
 static_assert(kTileTokens % (8 * kMaxCluster) == 0 && kTileTokens <= 256 && kChunkRows + 7 <= kTileTokens,
               "token tile");
 
@@ -167,11 +170,43 @@ struct Tables {
     const int32_t* eo;   // expert_offsets [E+1], global memory
 };
 
+// MODE of the single-launch decode kernel: FC1 with the SwiGLU epilogue as
+// pass 0, then FC2 with the weighted-store epilogue as pass 1, in one launch.
+constexpr int kFused = 3;
+
+// Loads of routing tables and FC2 epilogue inputs.  The other modes read data
+// that earlier launches wrote, through the read-only cache.  The fused kernel
+// writes them itself earlier in the same launch, before a grid barrier that
+// orders them (release / acquire at GPU scope); no SM reads these addresses
+// before that barrier, so no stale line can be cached, and an ordinary cached
+// load (ld.global.ca) sees the written values.
+template <int MODE, typename T>
+__device__ __forceinline__ T ld_table(const T* ptr) {
+    if (MODE == kFused) return __ldca(ptr);
+    return __ldg(ptr);
+}
+
+template <int MODE>
+__device__ __forceinline__ bool pass_fc1(int pass) {
+    return MODE == static_cast<int>(GemmEpilogue::SwiGLU) || (MODE == kFused && pass == 0);
+}
+
+// One GEMM pass of a launch: its parameters, tensor maps and work counts.
+struct Pass {
+    const KParams* p;
+    const GemmMaps* m;
+    int total;     // work units of the grid's clusters
+    int nq;        // K quads per tile
+    int ngroups;   // scale groups (kGroup quads) per tile
+    bool fc1;      // FC1 weight views (gate / up) and the SwiGLU epilogue
+};
+
 // Work unit u of a cluster -> (expert, feature-tile group, token chunk); the
 // CTA of cluster rank r takes feature tile group * cl + r.  Token chunks of
 // one (expert, feature-tile group) are adjacent so concurrent clusters share
 // weight tiles through L2.  chunk c of an expert with `cnt` rows split into
 // nc chunks covers rows [c*cnt/nc, (c+1)*cnt/nc).
+template <int MODE>
 __device__ __forceinline__ void decode_tile(const KParams& p, const Tables& tb, int u, int rank, TileInfo& ti) {
     const int v = u / p.nfg;
     int lo = 1, hi = p.E;                   // first e' with chunk_prefix[e'] > v
@@ -188,8 +223,8 @@ __device__ __forceinline__ void decode_tile(const KParams& p, const Tables& tb, 
     const int fg = local / nc;
     ti.f = fg * p.cl + rank;
     const int c = local - fg * nc;
-    const int off = __ldg(tb.eo + e);
-    const int cnt = __ldg(tb.eo + e + 1) - off;
+    const int off = ld_table<MODE>(tb.eo + e);
+    const int cnt = ld_table<MODE>(tb.eo + e + 1) - off;
     const int a = static_cast<int>(static_cast<long long>(c) * cnt / nc);
     const int b = static_cast<int>(static_cast<long long>(c + 1) * cnt / nc);
     const int r0 = off + a;
@@ -211,9 +246,8 @@ __device__ __forceinline__ uint32_t stage_bytes(const TileInfo& ti) {
 // [2] being row parity) (y, z) = (64 f, e); otherwise (view [E * rows_w][K])
 // y = e * rows_w + 128 f.  Either FC1 view lands the 64 gate rows and then
 // the 64 up rows in shared memory, so the MMA and epilogue are the same.
-template <int MODE>
-__device__ __forceinline__ void weight_coords(const KParams& p, const TileInfo& ti, int& y, int& z) {
-    if (MODE == static_cast<int>(GemmEpilogue::SwiGLU)) {
+__device__ __forceinline__ void weight_coords(bool fc1, const KParams& p, const TileInfo& ti, int& y, int& z) {
+    if (fc1) {
         y = ti.f * 64;
         z = p.interleaved ? ti.e : 2 * ti.e;
     } else {
@@ -350,19 +384,17 @@ __device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int x
 // Load (or prefetch) a box of the weight-scale / weight-prefetch maps: for
 // FC1 3-D (gate | up halves, z = 2e) or 4-D (interleaved rows, parity 0,
 // expert z); 2-D otherwise.
-template <int MODE>
-__device__ __forceinline__ void load_weight_box(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
-                                                int z, bool inter) {
-    if (MODE == static_cast<int>(GemmEpilogue::SwiGLU)) {
+__device__ __forceinline__ void load_weight_box(bool fc1, uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
+                                                int y, int z, bool inter) {
+    if (fc1) {
         if (inter) tma_load_4d(dst, map, bar, x, y, 0, z);
         else tma_load_3d(dst, map, bar, x, y, z);
     } else {
         tma_load_2d(dst, map, bar, x, y);
     }
 }
-template <int MODE>
-__device__ __forceinline__ void prefetch_weight_box(const CUtensorMap* map, int x, int y, int z, bool inter) {
-    if (MODE == static_cast<int>(GemmEpilogue::SwiGLU)) {
+__device__ __forceinline__ void prefetch_weight_box(bool fc1, const CUtensorMap* map, int x, int y, int z, bool inter) {
+    if (fc1) {
         if (inter) tma_prefetch_l2_4d(map, x, y, 0, z);
         else tma_prefetch_l2_3d(map, x, y, z);
     } else {
@@ -451,43 +483,98 @@ struct RingProducer {
     }
 };
 
-// Walks the (work unit, group of kGroup K quads) sequence of one CTA.
-template <int MODE>
+// Walks the (pass, work unit, group of kGroup K quads) sequence of one CTA:
+// every unit of pass 0, then every unit of pass 1.
+template <int MODE, int NP>
 struct GroupCursor {
-    int u, g;          // work unit and group index within the tile
+    int pass, u, g;    // pass, work unit and group index within the tile
     TileInfo ti;
     int wy, wz;
     bool valid;
-    int rank, stride;
+    int first, rank, stride;
     Tables tb;
-    __device__ __forceinline__ void start(const KParams& p, const Tables& tb_, int total, int first, int rank_,
-                                          int stride_) {
+    const Pass* P;
+    __device__ __forceinline__ void start(const Pass* P_, const Tables& tb_, int first_, int rank_, int stride_) {
+        P = P_;
         tb = tb_;
-        u = first;
+        first = first_;
         rank = rank_;
         stride = stride_;
+        pass = 0;
+        u = first;
         g = 0;
-        load(p, total);
+        load();
     }
-    __device__ __forceinline__ void load(const KParams& p, int total) {
-        valid = u < total;
+    __device__ __forceinline__ void load() {
+        while (pass < NP && u >= P[pass].total) {
+            ++pass;
+            u = first;
+        }
+        valid = pass < NP;
         if (valid) {
-            decode_tile(p, tb, u, rank, ti);
-            weight_coords<MODE>(p, ti, wy, wz);
+            decode_tile<MODE>(*P[pass].p, tb, u, rank, ti);
+            weight_coords(P[pass].fc1, *P[pass].p, ti, wy, wz);
         }
     }
-    __device__ __forceinline__ void advance(const KParams& p, int total, int ngroups) {
-        if (++g == ngroups) {
+    __device__ __forceinline__ void advance() {
+        if (++g == P[pass].ngroups) {
             g = 0;
             u += stride;
-            load(p, total);
+            load();
         }
     }
 };
 
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
-    mx_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ KParams p) {
+// Everything the fused decode kernel adds to the two GEMM passes: routing,
+// permutation and quantisation before them, the k-way combine after them,
+// and the counters of its grid barriers (all device pointers; the counters
+// are zero at launch).
+struct DecodeArgs {
+    const float* logits;
+    const uint16_t* hidden;
+    int T, H, E, k, renormalize;
+    int32_t* ids;
+    float* w;
+    int32_t* offsets;
+    int32_t* chunk_prefix;
+    int32_t* perm;
+    int32_t* inv_perm;
+    uint8_t* a1;
+    uint8_t* a1_sf;
+    int S4;
+    const uint16_t* y;
+    uint16_t* out;
+    unsigned* grid_ctr;   // grid barriers: barrier b completes at b * gridDim.x arrivals
+    unsigned* fc1_done;   // FC1 epilogue warps done: gridDim.x * 4 arrivals
+};
+
+// Spin (one thread) until *ctr reaches target, with a deadline; then make
+// the generic-proxy writes behind the counter visible to TMA loads.
+__device__ __forceinline__ bool wait_count(unsigned* ctr, unsigned target, volatile int* abort_flag, int* err,
+                                           uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) break;
+        if (*abort_flag || globaltimer_ns() - t0 > limit_ns) {
+            set_error(err, KT_DEVERR_TIMEOUT_GRID);
+            *abort_flag = 1;
+            return false;
+        }
+        __nanosleep(64);
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
+// The persistent warp-specialised GEMM over NP passes (NP = 1: one grouped
+// GEMM; NP = 2 with MODE kFused: FC1 then FC2 of the decode kernel, whose
+// prologue and combine phases also run here, d != nullptr).  M[i] and PP[i]
+// live in kernel parameter space.
+template <int MODE, int NP>
+__device__ __forceinline__ void gemm_body(const GemmMaps* M, const KParams* PP, const DecodeArgs* d) {
+    const KParams& p = PP[0];   // fields every pass shares (E, cl, tables, error word, wait limits)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -528,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(empty_bar(s), cl);    // one tcgen05.commit per CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(sf_full(b), 32);      // one arrive per scale-warp lane
+            mbar_init(sf_full(b), 1);       // the scale warp's tcgen05.commit of its scale copies
             mbar_init(sf_empty(b), 1);      // tcgen05.commit
             mbar_init(acc_full(b), 1);      // tcgen05.commit
             mbar_init(acc_empty(b), 4);     // one arrive per epilogue warp
@@ -542,24 +629,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the first global-memory access: the previous kernel in the stream has completed
     griddep_wait();
     griddep_launch_dependents();
-    for (int i = threadIdx.x; i <= p.E; i += kThreads) {
-        s_cp[i] = __ldg(p.chunk_prefix + i);
+    if (MODE != kFused) {
+        for (int i = threadIdx.x; i <= p.E; i += kThreads) s_cp[i] = __ldg(p.chunk_prefix + i);
     }
     if (warp == 1) {
         tc_alloc(smem_u32(tmem_slot), kTmemCols);
         tc_relinquish();
     }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&maps.w[0]);
-        tma_prefetch_map(&maps.w[1]);
-    }
-    if (warp == 3) {
-        for (int i = lane; i < 2 * kMaxShare; i += 32) tma_prefetch_map(&maps.t[i / kMaxShare][i % kMaxShare]);
-    }
-    if (warp == 2 && lane == 0) {
-        tma_prefetch_map(&maps.wpf);
-        tma_prefetch_map(&maps.asf);
-        if (p.sfa_tma) tma_prefetch_map(&maps.wsf);
+    for (int i = 0; i < NP; ++i) {
+        const GemmMaps& mm = M[i];
+        if (warp == 0 && lane == 0) {
+            tma_prefetch_map(&mm.w[0]);
+            tma_prefetch_map(&mm.w[1]);
+        }
+        if (warp == 3) {
+            for (int j = lane; j < 2 * kMaxShare; j += 32) tma_prefetch_map(&mm.t[j / kMaxShare][j % kMaxShare]);
+        }
+        if (warp == 2 && lane == 0) {
+            tma_prefetch_map(&mm.wpf);
+            tma_prefetch_map(&mm.asf);
+            if (PP[i].sfa_tma) tma_prefetch_map(&mm.wsf);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -567,9 +657,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int total = p.nfg * s_cp[p.E];   // work units of the grid's clusters
-    const int nq = p.K / 128;                  // K quads per tile
-    const int ngroups = (nq + kGroup - 1) / kGroup;
+    if (MODE == kFused) {
+        // ---------------------------------------------------------- decode prologue
+        // route (a warp per token), grid barrier, permute (CTA 0, the stage ring as
+        // scratch), grid barrier, quantise A1 (a warp per token), grid barrier; then
+        // every CTA stages chunk_prefix like the other modes.
+        const int nw = kThreads / 32;
+        const int gw = static_cast<int>(blockIdx.x) * nw + warp;
+        const int nwg = static_cast<int>(gridDim.x) * nw;
+        const unsigned g = gridDim.x;
+        const int S = d->T * d->k;
+        int* s_warp = reinterpret_cast<int*>(epi);        // 33 ints
+        for (int t = gw; t < d->T; t += nwg)
+            route_token_warp(d->logits + static_cast<size_t>(t) * d->E, d->E, d->k, d->renormalize,
+                             d->ids + static_cast<size_t>(t) * d->k, d->w + static_cast<size_t>(t) * d->k);
+        grid_barrier(d->grid_ctr, 1 * g, abort_flag, p.err, p.wait_limit_ns);
+        if (blockIdx.x == 0 && !*abort_flag)
+            permute_block(d->ids, S, d->E, d->offsets, d->chunk_prefix, d->perm, d->inv_perm, p.err,
+                          reinterpret_cast<int*>(smem), s_warp);
+        grid_barrier(d->grid_ctr, 2 * g, abort_flag, p.err, p.wait_limit_ns);
+        if (!*abort_flag) {
+            int* s_dst = reinterpret_cast<int*>(epi) + 64 + warp * kMaxTopK;
+            for (int t = gw; t < d->T; t += nwg)
+                quant_token_warp(d->hidden, t, d->H, d->k, d->inv_perm, d->a1, d->a1_sf, d->S4, s_dst);
+        }
+        grid_barrier(d->grid_ctr, 3 * g, abort_flag, p.err, p.wait_limit_ns);
+        for (int i = threadIdx.x; i <= p.E; i += kThreads) s_cp[i] = __ldcg(d->chunk_prefix + i);
+        __syncthreads();
+    }
+
+    Pass P[NP];
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+        P[i].p = &PP[i];
+        P[i].m = &M[i];
+        P[i].total = *abort_flag ? 0 : PP[i].nfg * s_cp[p.E];   // work units of the grid's clusters
+        P[i].nq = PP[i].K / 128;
+        P[i].ngroups = (P[i].nq + kGroup - 1) / kGroup;
+        P[i].fc1 = pass_fc1<MODE>(i);
+    }
 
     if (warp == 0 || warp == 3) {
         // ------------------------------------------------------------ producers (one lane each)
@@ -584,17 +710,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_a = l2_policy_evict_last();
             RingProducer rp;
             long long gi = 0;
-            for (int u = first; u < total && ok; u += stride) {
+            for (int pass = 0; pass < NP && ok; ++pass) {
+            const Pass& ps = P[pass];
+            const KParams& pp = *ps.p;
+            const GemmMaps& mm = *ps.m;
+            const int nq = ps.nq;
+            // FC2 token rows (A2) are written by every CTA's FC1 epilogue in this launch
+            if (MODE == kFused && pass == 1 && !weights)
+                ok = wait_count(d->fc1_done, gridDim.x * 4u, abort_flag, p.err, p.wait_limit_ns);
+            for (int u = first; u < ps.total && ok; u += stride) {
                 TileInfo ti;
-                decode_tile(p, tb, u, rank, ti);
+                decode_tile<MODE>(pp, tb, u, rank, ti);
                 int wy, wz;
-                weight_coords<MODE>(p, ti, wy, wz);
+                weight_coords(ps.fc1, pp, ti, wy, wz);
                 const uint32_t need = stage_bytes(ti);
                 const int nk = (nq + ti.kqs - 1) / ti.kqs;
                 const int share = (ti.nmma >> 3) / cl;            // 8-row groups this CTA loads
                 const int g0 = (ti.r_al >> 3) + rank * share;
                 const uint32_t gstride = static_cast<uint32_t>(ti.kqs) * 1024u;   // bytes per 8-row group
-                const CUtensorMap* tm = &maps.t[ti.kqs - 1][share - 1];   // one box covers this CTA's share
+                const CUtensorMap* tm = &mm.t[ti.kqs - 1][share - 1];   // one box covers this CTA's share
                 for (int kb = 0; kb < nk; ++kb, ++gi) {
                     const uint64_t start = rp.acquire(gi, need, empty_base, abort_flag, p.wait_limit_ns);
                     if (start == ~0ull) {
@@ -602,16 +736,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const int slot = static_cast<int>(gi % kSlots);
-                    const bool withhold = (p.debug_flags & KT_DEBUG_WITHHOLD_STAGE) && u == first && kb == 0;
+                    const bool withhold =
+                        (p.debug_flags & KT_DEBUG_WITHHOLD_STAGE) && pass == 0 && u == first && kb == 0;
                     if (withhold) continue;   // test hook: a withheld stage is neither loaded nor signalled
                     const uint32_t dst = ring_base + static_cast<uint32_t>(start % kRing);
                     const int kq0 = kb * ti.kqs;
                     if (weights) {
                         mbar_arrive_expect_tx(full_bar(slot), kQuadWTx * ti.kqs);
-                        const CUtensorMap* wm = &maps.w[ti.kqs - 1];
-                        if (MODE == static_cast<int>(GemmEpilogue::SwiGLU) && p.interleaved)
+                        const CUtensorMap* wm = &mm.w[ti.kqs - 1];
+                        if (ps.fc1 && pp.interleaved)
                             tma_load_5d_hint(dst, wm, full_bar(slot), 0, wy, 0, wz, kq0, pol_w);
-                        else if (MODE == static_cast<int>(GemmEpilogue::SwiGLU))
+                        else if (ps.fc1)
                             tma_load_4d_hint(dst, wm, full_bar(slot), 0, wy, wz, kq0, pol_w);
                         else
                             tma_load_3d_hint(dst, wm, full_bar(slot), 0, wy, kq0, pol_w);
@@ -627,6 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            }
             if (!ok) {
                 set_error(p.err, KT_DEVERR_TIMEOUT_LOAD);
                 *abort_flag = 1;
@@ -640,30 +776,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sw = warp == 2 ? 0 : 1;
         uint32_t stg_ph = 0u, sfe_ph = 0u;   // one parity bit per buffer
         bool ok = true;
-        const uint32_t stg_tx = static_cast<uint32_t>(kStgSFB + (p.sfa_tma ? kStgSFA : 0));
-        const int ksf = p.K / 32;
-        GroupCursor<MODE> cur, ahead, pf;
-        cur.start(p, tb, total, first, rank, stride);
-        if (sw) cur.advance(p, total, ngroups);
+        bool a2_ready = MODE != kFused;      // fused: FC2's token scales exist once every FC1 epilogue is done
+        GroupCursor<MODE, NP> cur, ahead, pf;
+        cur.start(P, tb, first, rank, stride);
+        if (sw) cur.advance();
         ahead = cur;
         pf = cur;
-        auto advance2 = [&](GroupCursor<MODE>& c) {
-            c.advance(p, total, ngroups);
-            c.advance(p, total, ngroups);
+        auto advance2 = [&](GroupCursor<MODE, NP>& c) {
+            c.advance();
+            c.advance();
         };
-        auto issue_staging = [&](const GroupCursor<MODE>& c, int buf) {
+        // Fused kernel: the staging of the first FC2 group is deferred until that group is the one
+        // being built, and then waits for every CTA's FC1 epilogue.  (Waiting when it is issued, a
+        // group ahead, would hold back this CTA's last FC1 group, and with it every CTA's FC2.)
+        GroupCursor<MODE, NP> deferred;
+        int deferred_buf = -1;
+        auto issue_staging = [&](const GroupCursor<MODE, NP>& c, int buf) {
+            if (MODE == kFused && c.valid && c.pass == 1 && !a2_ready) {
+                deferred = c;
+                deferred_buf = buf;
+                return;
+            }
             if (lane == 0 && c.valid) {
+                const KParams& pp = *P[c.pass].p;
+                const GemmMaps& mm = *P[c.pass].m;
                 const uint32_t dst = smem_u32(stg + buf * kStgBytes);
                 fence_proxy_async_smem();
-                mbar_arrive_expect_tx(stg_bar(buf), stg_tx);
-                if (p.sfa_tma)
-                    load_weight_box<MODE>(dst, &maps.wsf, stg_bar(buf), c.g * 16, c.wy, c.wz, p.interleaved != 0);
-                tma_load_2d(dst + kStgSFA, &maps.asf, stg_bar(buf), c.ti.r_al, c.g * kGroup);
+                mbar_arrive_expect_tx(stg_bar(buf), static_cast<uint32_t>(kStgSFB + (pp.sfa_tma ? kStgSFA : 0)));
+                if (pp.sfa_tma)
+                    load_weight_box(P[c.pass].fc1, dst, &mm.wsf, stg_bar(buf), c.g * 16, c.wy, c.wz,
+                                    pp.interleaved != 0);
+                tma_load_2d(dst + kStgSFA, &mm.asf, stg_bar(buf), c.ti.r_al, c.g * kGroup);
             }
         };
-        auto prefetch_group = [&](const GroupCursor<MODE>& c) {
+        auto prefetch_group = [&](const GroupCursor<MODE, NP>& c) {
             if (lane == 0 && c.valid)
-                prefetch_weight_box<MODE>(&maps.wpf, c.g * (kGroup * 128 / 2), c.wy, c.wz, p.interleaved != 0);
+                prefetch_weight_box(P[c.pass].fc1, &P[c.pass].m->wpf, c.g * (kGroup * 128 / 2), c.wy, c.wz,
+                                    P[c.pass].p->interleaved != 0);
         };
         for (int i = 0; i < kPrefetchGroups; ++i) {   // this warp's next groups
             prefetch_group(pf);
@@ -676,6 +825,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int sbuf = 2 * sw + (lidx & 1);   // staging buffer of this group
             const int fbuf = sw;                    // scale-block buffer of this group
             __syncwarp();                           // every lane is done with the buffer refilled next
+            if (MODE == kFused && deferred_buf >= 0) {
+                // the deferred group is this one (it was staged into sbuf's turn): every earlier group of
+                // this warp is built, so wait for every CTA's A2 and stage it before the next is staged
+                bool ready = true;
+                if (lane == 0) ready = wait_count(d->fc1_done, gridDim.x * 4u, abort_flag, p.err, p.wait_limit_ns);
+                ok = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                a2_ready = true;
+                issue_staging(deferred, deferred_buf);
+                deferred_buf = -1;
+            }
             issue_staging(ahead, 2 * sw + ((lidx + 1) & 1));
             advance2(ahead);
             prefetch_group(pf);
@@ -687,6 +847,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    p.wait_limit_ns));
             if (!ok) break;
             const TileInfo& ti = cur.ti;
+            const KParams& pp = *P[cur.pass].p;
+            const int nq = P[cur.pass].nq;
+            const int ksf = pp.K / 32;
             const uint8_t* sb = stg + sbuf * kStgBytes;
             uint8_t* sfo = sfbuf + fbuf * kSfBytes;
             const int kq0 = cur.g * kGroup;
@@ -696,7 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // weight scales: staging row r holds the 16 scale bytes of the group (word kk = quad kk); one
             // 16-byte load per row serves all four quads (consecutive rows per lane: no bank conflicts)
             uint4 wrow[4];
-            if (p.sfa_tma) {
+            if (pp.sfa_tma) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) wrow[i] = *reinterpret_cast<const uint4*>(sb + (lane + 32 * i) * 16);
             }
@@ -705,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kk >= nkk) break;
                 uint8_t* blk = sfo + kk * kSfQuad;
                 // tile row r -> byte (r%32)*16 + (r/32)*4 of the 512-byte block
-                if (p.sfa_tma) {
+                if (pp.sfa_tma) {
                     auto word = [&](const uint4& v) { return kk == 0 ? v.x : kk == 1 ? v.y : kk == 2 ? v.z : v.w; };
                     *reinterpret_cast<uint4*>(blk + lane * 16) =
                         make_uint4(word(wrow[0]), word(wrow[1]), word(wrow[2]), word(wrow[3]));
@@ -714,13 +877,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 4; ++i) {
                         const int r = lane + 32 * i;
                         size_t grow;
-                        if (MODE == static_cast<int>(GemmEpilogue::SwiGLU) && p.interleaved)
-                            grow = static_cast<size_t>(ti.e) * p.rows_w + 2 * (ti.f * 64 + (r & 63)) + (r < 64 ? 0 : 1);
-                        else if (MODE == static_cast<int>(GemmEpilogue::SwiGLU))
-                            grow = static_cast<size_t>(ti.e) * p.rows_w + (r < 64 ? 0 : p.I) + ti.f * 64 + (r & 63);
+                        if (P[cur.pass].fc1 && pp.interleaved)
+                            grow = static_cast<size_t>(ti.e) * pp.rows_w + 2 * (ti.f * 64 + (r & 63)) + (r < 64 ? 0 : 1);
+                        else if (P[cur.pass].fc1)
+                            grow = static_cast<size_t>(ti.e) * pp.rows_w + (r < 64 ? 0 : pp.I) + ti.f * 64 + (r & 63);
                         else
-                            grow = static_cast<size_t>(ti.e) * p.rows_w + ti.f * 128 + r;
-                        cp_async_4(smem_u32(blk + lane * 16 + i * 4), p.w_sf + grow * ksf + (kq0 + kk) * 4, 4);
+                            grow = static_cast<size_t>(ti.e) * pp.rows_w + ti.f * 128 + r;
+                        cp_async_4(smem_u32(blk + lane * 16 + i * 4), pp.w_sf + grow * ksf + (kq0 + kk) * 4, 4);
                     }
                 }
                 // token scales from the K-step-major staging rows (tile column t = row r_al + t)
@@ -736,9 +899,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         make_uint4(t4[0], t4[1], t4[2], t4[3]);
                 }
             }
+            // The scale warp copies the group's blocks into its tensor-memory scale buffer itself
+            // (tcgen05.cp), and the copies' commit completes sf_full: the MMA warp then issues
+            // nothing but MMAs.  Each copy puts one 32-row x 16-byte block into all four lane
+            // quadrants, the layout block-scaled MMAs read scale factors from.
+            if (!pp.sfa_tma) asm volatile("cp.async.wait_all;" ::: "memory");
             fence_proxy_async_smem();
-            if (p.sfa_tma) mbar_arrive(sf_full(fbuf));
-            else cp_async_arrive_noinc(sf_full(fbuf));
+            __syncwarp();
+            tc_fence_after();
+            if (elect_one_sync()) {
+                const uint64_t dF0 = sdesc_sf_block(smem_u32(sfo));
+                const uint32_t t_buf = tmem + kTmemSF + static_cast<uint32_t>(fbuf) * kSfGroupCols;
+                for (int kk = 0; kk < nkk; ++kk) {
+                    const uint64_t dF = dF0 + static_cast<uint64_t>((kk * kSfQuad) >> 4);
+                    const uint32_t t_sfa = t_buf + static_cast<uint32_t>(kk) * kSfQuadCols;
+                    tc_cp_32x128b_warpx4(t_sfa, dF);
+                    tc_cp_32x128b_warpx4(t_sfa + 4, dF + (512 >> 4));
+                    if (natoms > 1) tc_cp_32x128b_warpx4(t_sfa + 8, dF + (1024 >> 4));
+                }
+                tc_commit(sf_full(fbuf));
+            }
+            __syncwarp();
             stg_ph ^= 1u << sbuf;
             sfe_ph ^= 1u << fbuf;
             ++lidx;
@@ -759,13 +940,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto leader = [&]() -> bool { return elect_one_sync(); };
             auto wsync = [&]() { __syncwarp(); };
             int sb = 0, it = 0;
-            long long gi = 0;
+            int slot = 0;                       // pipeline slot of the next stage ...
+            uint32_t full_ph = 0u;              // ... and the parity its full barrier completes with
             PhysRing ring;
             uint32_t acc_ph = 0u, sf_ph = 0u;   // one parity bit per buffer
             bool ok = true, issued = false;
-            for (int u = first; u < total && ok; u += stride, ++it) {
+            // Shared-memory descriptors with a zero start address: a stage adds its address >> 4
+            // (bits 0-13; shared addresses stay below 256 KB, so nothing carries out), and each
+            // 32-byte K step of a quad adds 2.  The issuing lane runs alone, so its instruction
+            // chain is kept short: no descriptor is rebuilt inside the stage loop.
+            const uint64_t dA_t = sdesc_sw128_sbo(0u, 1024);
+            for (int pass = 0; pass < NP && ok; ++pass) {
+            const int nq = P[pass].nq;
+            for (int u = first; u < P[pass].total && ok; u += stride, ++it) {
                 TileInfo ti;
-                decode_tile(p, tb, u, rank, ti);
+                decode_tile<MODE>(*P[pass].p, tb, u, rank, ti);
                 const int ab = it & 1;
                 issued = true;
                 ok = wait(acc_empty(ab), ((acc_ph >> ab) & 1u) ^ 1u);
@@ -775,53 +964,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t idesc0 = idesc_mx_e2m1_e4m3(ti.nmma, 0);
                 const uint32_t need = stage_bytes(ti);
                 const int nk = (nq + ti.kqs - 1) / ti.kqs;
-                const uint32_t tok_sbo = static_cast<uint32_t>(ti.kqs) * 1024u;
-                for (int kb = 0; kb < nk && ok; ++kb, ++gi) {
+                const uint64_t dB_t = sdesc_sw128_sbo(0u, static_cast<uint32_t>(ti.kqs) * 1024u);
+                const uint32_t b_off16 = static_cast<uint32_t>(ti.kqs * kQuadW) >> 4;
+                for (int kb = 0; kb < nk && ok; ++kb) {
                     const uint32_t off = ring.place(need);
-                    const int slot = static_cast<int>(gi % kSlots);
                     const int kq0 = kb * ti.kqs;
                     const int nqs = min(ti.kqs, nq - kq0);     // K quads in this stage
                     const int kq_last = kq0 + nqs - 1;
                     // a stage never straddles scale groups: it starts a group when kq0 % kGroup == 0
                     const bool group_start = (kq0 & (kGroup - 1)) == 0;
                     const bool group_end = (kq_last & (kGroup - 1)) == kGroup - 1 || kq_last == nq - 1;
-                    ok = wait(full_bar(slot), static_cast<uint32_t>((gi / kSlots) & 1));
+                    ok = wait(full_bar(slot), full_ph);
                     if (!ok) break;
-                    if (group_start) {
+                    if (group_start) {   // the group's scales are in tensor memory
                         ok = wait(sf_full(sb), (sf_ph >> sb) & 1u);
                         if (!ok) break;
-                        // blocks gathered by cp.async were written through the generic proxy; the
-                        // TMA-staged path fences on the writer's side before it arrives
-                        if (!p.sfa_tma) fence_proxy_async_smem();
                     }
                     tc_fence_after();
                     if (leader()) {
-                        for (int q = 0; q < nqs; ++q) {
-                            const int kk = (kq0 + q) & (kGroup - 1);
-                            const uint32_t sA = ring_base + off + q * kQuadW;
-                            const uint32_t sB = ring_base + off + ti.kqs * kQuadW + q * 1024;
-                            const uint32_t sF = smem_u32(sfbuf + sb * kSfBytes + kk * kSfQuad);
-                            const uint32_t t_sfa = tmem + kTmemSF + slot * kSfSlotCols + q * 12;
-                            const uint32_t t_sfb = t_sfa + 4;
-                            const uint64_t dF = sdesc_sf_block(sF);
-                            tc_cp_32x128b_warpx4(t_sfa, dF);
-                            tc_cp_32x128b_warpx4(t_sfb, dF + (512 >> 4));
-                            if (ti.nmma > 128) tc_cp_32x128b_warpx4(t_sfb + 4, dF + (1024 >> 4));
-                            // descriptors built once per quad; each 32-byte K step adds 2 to
-                            // the start-address field (bits 0-13, address >> 4; no carry out
-                            // below 256 KB of shared memory)
-                            const uint64_t dA = sdesc_sw128_sbo(sA, 1024);
-                            const uint64_t dB = sdesc_sw128_sbo(sB, tok_sbo);
-                            const bool first_quad = (kq0 + q) == 0;
+                        const uint64_t sa = static_cast<uint64_t>((ring_base + off) >> 4);
+                        const uint32_t t_sf = tmem + kTmemSF + static_cast<uint32_t>(sb) * kSfGroupCols;
+                        auto issue_quad = [&](int q) {
+                            const int kq = kq0 + q;
+                            const uint32_t t_sfa = t_sf + static_cast<uint32_t>(kq & (kGroup - 1)) * kSfQuadCols;
+                            const uint64_t dA = dA_t + sa + static_cast<uint64_t>(q * (kQuadW >> 4));
+                            const uint64_t dB = dB_t + sa + b_off16 + static_cast<uint64_t>(q * (1024 >> 4));
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 const uint32_t idesc =
                                     idesc0 | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
-                                const bool fresh = first_quad && j == 0;
                                 tc_mma_mxf8f6f4(d_tmem, dA + static_cast<uint64_t>(2 * j),
-                                                dB + static_cast<uint64_t>(2 * j), idesc, t_sfa, t_sfb, fresh ? 0u : 1u);
+                                                dB + static_cast<uint64_t>(2 * j), idesc, t_sfa, t_sfa + 4,
+                                                (kq == 0 && j == 0) ? 0u : 1u);
                             }
-                        }
+                        };
+                        issue_quad(0);
+                        if (nqs > 1) issue_quad(1);
                         if (group_end) tc_commit(sf_empty(sb));
                         if (cl > 1) tc_commit_mc(empty_bar(slot), cl_mask);   // frees the stage in every CTA
                         else tc_commit(empty_bar(slot));
@@ -831,11 +1009,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sf_ph ^= 1u << sb;
                         sb ^= 1;
                     }
+                    if (++slot == kSlots) {
+                        slot = 0;
+                        full_ph ^= 1u;
+                    }
                 }
                 if (!ok) break;
                 if (leader()) tc_commit(acc_full(ab));
                 wsync();
                 acc_ph ^= 1u << ab;
+            }
             }
             if (!ok) {
                 if (lane == 0) set_error(p.err, KT_DEVERR_TIMEOUT_MMA);
@@ -854,9 +1037,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc_ph = 0u;                          // one parity bit per buffer
         int it = 0;
         bool ok = true;
-        for (int u = first; u < total && ok; u += stride, ++it) {
+        for (int pass = 0; pass < NP; ++pass) {
+        const KParams& pp = *P[pass].p;
+        const int ek = MODE == kFused ? (pass == 0 ? static_cast<int>(GemmEpilogue::SwiGLU)
+                                                   : static_cast<int>(GemmEpilogue::Combine))
+                                      : MODE;
+        for (int u = first; u < P[pass].total && ok; u += stride, ++it) {
             TileInfo ti;
-            decode_tile(p, tb, u, rank, ti);
+            decode_tile<MODE>(pp, tb, u, rank, ti);
             const int ab = it & 1;
             ok = __all_sync(0xffffffffu, mbar_wait(acc_full(ab), (acc_ph >> ab) & 1u, abort_flag, p.wait_limit_ns));
             if (!ok) break;
@@ -867,14 +1055,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[32];
                 tc_ld_32x32b_x32(trow + static_cast<uint32_t>(c0), v);
                 tc_wait_ld();
-                if (MODE == static_cast<int>(GemmEpilogue::Raw)) {
+                if (ek == static_cast<int>(GemmEpilogue::Raw)) {
                     const int n = ti.f * 128 + q * 32 + lane;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         if (c0 + j >= lo && c0 + j < hi)
-                            p.raw_out[static_cast<size_t>(ti.r_al + c0 + j) * p.rows_w + n] = __uint_as_float(v[j]);
+                            pp.raw_out[static_cast<size_t>(ti.r_al + c0 + j) * pp.rows_w + n] = __uint_as_float(v[j]);
                     }
-                } else if (MODE == static_cast<int>(GemmEpilogue::Combine)) {
+                } else if (ek == static_cast<int>(GemmEpilogue::Combine)) {
                     // weight, round to bf16 and transpose through shared memory so each
                     // lane writes 64 contiguous bytes of one token's output row
                     uint8_t* tb = epi + q * 2560;   // [32 tokens][80 bytes]
@@ -882,8 +1070,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int slot = 0;
                     float wt = 0.f;
                     if (mine) {
-                        slot = __ldg(p.perm + ti.r_al + c0 + lane);
-                        wt = __ldg(p.topk_w + slot);
+                        slot = ld_table<MODE>(pp.perm + ti.r_al + c0 + lane);
+                        wt = ld_table<MODE>(pp.topk_w + slot);
                     }
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -903,7 +1091,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int mk = __shfl_sync(0xffffffffu, mine_i, tk);
                         if (mk) {
                             const uint4 val = *reinterpret_cast<const uint4*>(tb + tk * 80 + (lane & 3) * 16);
-                            uint4* dst = reinterpret_cast<uint4*>(p.y + static_cast<size_t>(sl) * p.H + ti.f * 128 +
+                            uint4* dst = reinterpret_cast<uint4*>(pp.y + static_cast<size_t>(sl) * pp.H + ti.f * 128 +
                                                                   q * 32) +
                                          (lane & 3);
                             *dst = val;
@@ -919,8 +1107,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool gate = q < 2;
                     float* X = reinterpret_cast<float*>(epi) + pair * 512;          // silu(gate), columns 16-31
                     float* Y = reinterpret_cast<float*>(epi) + 1024 + pair * 512;   // up, columns 0-15
-                    const int act = p.act;
-                    const float alpha = p.alpha, limit = p.limit;
+                    const int act = pp.act;
+                    const float alpha = pp.alpha, limit = pp.limit;
                     if (gate) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
@@ -958,11 +1146,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const size_t row = static_cast<size_t>(ti.r_al + col_t);
                         const int col = ti.f * 64 + pair * 32;
                         const uint4* srcv = reinterpret_cast<const uint4*>(my_bt + lane * 32);
-                        uint4* dst = reinterpret_cast<uint4*>(p.a2 + row * p.I + col);
+                        uint4* dst = reinterpret_cast<uint4*>(pp.a2 + row * pp.I + col);
                         dst[0] = srcv[0];
                         dst[1] = srcv[1];
                         const int blk = col >> 5;
-                        p.a2_sf[((static_cast<size_t>(blk >> 2) * p.S4 + row) << 2) + (blk & 3)] = my_scale;
+                        pp.a2_sf[((static_cast<size_t>(blk >> 2) * pp.S4 + row) << 2) + (blk & 3)] = my_scale;
                     }
                     named_bar_sync(2, 128);
                 }
@@ -972,6 +1160,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(acc_empty(ab));
             acc_ph ^= 1u << ab;
         }
+        if (MODE == kFused && pass == 0) {
+            // this warp's A2 rows are written: make them visible to every CTA's FC2 TMA loads
+            __syncwarp();
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __threadfence();
+                atomicAdd(d->fc1_done, 1u);
+            }
+        }
+        }
         if (!ok) {
             if (lane == 0) set_error(p.err, KT_DEVERR_TIMEOUT_EPI);
             *abort_flag = 1;
@@ -980,6 +1178,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (MODE == kFused) {
+        // ---------------------------------------------------------- decode combine
+        // every CTA's FC2 epilogue has written its weighted rows y: out[t] = sum_j y[t*k + j]
+        grid_barrier(d->grid_ctr, 4 * gridDim.x, abort_flag, p.err, p.wait_limit_ns);
+        if (!*abort_flag)
+            combine_rows<true>(d->y, d->ids, d->T, d->H, d->k, d->E, d->out,
+                               static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x,
+                               static_cast<long long>(gridDim.x) * kThreads);
+    }
     if (*abort_flag) __nanosleep(1000000);   // let any copy or commit still in flight land before teardown
     // no CTA leaves while a peer may still multicast into it or arrive on its barriers
     if (cl > 1) cluster_sync_all();
@@ -987,6 +1194,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tc_dealloc(tmem, kTmemCols);
     }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ KParams p) {
+    gemm_body<MODE, 1>(&maps, &p, nullptr);
+}
+
+// The single-launch decode kernel: routing, permutation, quantisation, FC1,
+// FC2 and the combine, as one cooperative launch with one CTA per SM.
+struct DecodeParams {
+    GemmMaps maps[2];
+    KParams p[2];
+    DecodeArgs d;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_constant__ DecodeParams dp) {
+    gemm_body<kFused, 2>(dp.maps, dp.p, &dp.d);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1267,15 +1492,14 @@ static bool get_maps(const GemmArgs& a, GemmMaps& maps) {
     return true;
 }
 
-kt_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
-    if (a.S <= 0) return KT_OK;
-    alignas(64) GemmMaps maps;
+// Kernel parameters of one GEMM pass (cluster size and feature-tile groups
+// are set by the launcher).
+static void fill_params(const GemmArgs& a, KParams& kp) {
     const bool fc1 = a.mode == GemmEpilogue::SwiGLU;
     const bool inter = fc1 && a.interleaved;
     const int S4 = sf_rows(a.S);
     const bool sfa_tma = (a.K % 512) == 0;
-    if (!get_maps(a, maps)) return report(KT_ERR_CUDA, "tensor map encoding failed");
-    KParams kp{};
+    kp = KParams{};
     kp.expert_offsets = a.expert_offsets;
     kp.chunk_prefix = a.chunk_prefix;
     kp.E = a.E;
@@ -1302,6 +1526,16 @@ kt_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
     kp.act = fc1 ? a.activation : 0;
     kp.alpha = a.alpha;
     kp.limit = a.limit;
+    kp.cl = 1;
+    kp.nfg = kp.n_ftiles;
+}
+
+kt_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
+    if (a.S <= 0) return KT_OK;
+    alignas(64) GemmMaps maps;
+    if (!get_maps(a, maps)) return report(KT_ERR_CUDA, "tensor map encoding failed");
+    KParams kp;
+    fill_params(a, kp);
     const int max_cluster = kGemmMaxCluster;
     cudaError_t e;
     switch (a.mode) {
@@ -1310,6 +1544,58 @@ kt_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
         default: e = launch_mode<2>(maps, kp, max_cluster, s); break;
     }
     return cuda_status(e);
+}
+
+kt_status launch_decode(const GemmArgs& fc1, const GemmArgs& fc2, const DecodeInputs& in, cudaStream_t s) {
+    alignas(64) DecodeParams dp;
+    if (!get_maps(fc1, dp.maps[0]) || !get_maps(fc2, dp.maps[1]))
+        return report(KT_ERR_CUDA, "tensor map encoding failed");
+    fill_params(fc1, dp.p[0]);
+    fill_params(fc2, dp.p[1]);
+    DecodeArgs& d = dp.d;
+    d.logits = in.logits;
+    d.hidden = in.hidden;
+    d.T = in.T;
+    d.H = in.H;
+    d.E = in.E;
+    d.k = in.k;
+    d.renormalize = in.renormalize;
+    d.ids = in.ids;
+    d.w = in.w;
+    d.offsets = in.offsets;
+    d.chunk_prefix = in.chunk_prefix;
+    d.perm = in.perm;
+    d.inv_perm = in.inv_perm;
+    d.a1 = in.a1;
+    d.a1_sf = in.a1_sf;
+    d.S4 = sf_rows(static_cast<long long>(in.T) * in.k);
+    d.y = in.y;
+    d.out = in.out;
+    d.grid_ctr = in.grid_ctr;
+    d.fc1_done = in.fc1_done;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(moe_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   kSmemTotal);
+        if (e != cudaSuccess) return cuda_status(e);
+        attr_set[dev] = true;
+    }
+    // one CTA per SM, all resident at once (cooperative): the kernel's grid barriers wait on every CTA
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(sm_count()));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemTotal;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, moe_decode_kernel, dp);
+    count_launches(1);
+    return cuda_status(e != cudaSuccess ? e : cudaGetLastError());
 }
 
 }  // namespace kt

@@ -131,6 +131,29 @@ DebugSettings debug_settings();
 // Returns KT_OK, KT_ERR_CUDA (launch / map encoding failure).
 kt_status launch_gemm(const GemmArgs& a, cudaStream_t s);
 
+// The single-launch decode kernel (route -> permute -> quantise -> FC1 ->
+// FC2 -> combine), for T * k <= kDecodeMaxSlots slots.  fc1 / fc2 are the two
+// GEMM passes as launch_gemm takes them (their routing tables are written by
+// the kernel itself); grid_ctr and fc1_done are zeroed device counters.
+struct DecodeInputs {
+    const float* logits;
+    const uint16_t* hidden;
+    int T, H, E, k, renormalize;
+    int32_t* ids;
+    float* w;
+    int32_t* offsets;
+    int32_t* chunk_prefix;
+    int32_t* perm;
+    int32_t* inv_perm;
+    uint8_t* a1;
+    uint8_t* a1_sf;
+    const uint16_t* y;
+    uint16_t* out;
+    unsigned* grid_ctr;
+    unsigned* fc1_done;
+};
+kt_status launch_decode(const GemmArgs& fc1, const GemmArgs& fc2, const DecodeInputs& in, cudaStream_t s);
+
 // Device properties cached per device.
 int sm_count();
 

@@ -8,16 +8,11 @@
 // nearest-even, saturating at +-448.
 #include "kt_common.cuh"
 #include "kt_internal.h"
+#include "kt_quant_dev.cuh"
 
 namespace kt {
 
-// One warp per token row.  Lane l quantises 32-element blocks l, l+32, ...
-// (64 contiguous input bytes each); the 32 codes + scale byte go to every
-// permuted row the token's k slots map to.  The codes of a pass of 32 blocks
-// (1 KB per row) are exchanged through shuffles once, so that each store
-// instruction writes 512 contiguous bytes of a row: one 16-byte store per
-// lane at a 32-byte stride left half-filled sectors and measured 25-33 %
-// slower on GB300.
+// One warp per token row (quant_token_warp in kt_quant_dev.cuh).
 __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __restrict__ hidden, int T, int H, int k,
                                                             const int32_t* __restrict__ inv_perm,
                                                             uint8_t* __restrict__ a1, uint8_t* __restrict__ a1_sf,
@@ -26,98 +21,9 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
     griddep_launch_dependents();
     __shared__ int s_dst[8][kMaxTopK];
     const int wib = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + wib;
     if (t >= T) return;   // whole warp
-    if (lane < k) s_dst[wib][lane] = inv_perm[static_cast<size_t>(t) * k + lane];
-    __syncwarp();
-    const int nblk = H >> 5;
-    const uint16_t* row = hidden + static_cast<size_t>(t) * H;
-    // warp-uniform passes of 32 blocks: lane l converts block b0 + l (if it
-    // exists); the next pass's block is loaded before this one is converted
-    uint4 nxt[4] = {};
-    if (lane < nblk) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) nxt[i] = __ldcs(reinterpret_cast<const uint4*>(row + lane * 32) + i);
-    }
-    for (int b0 = 0; b0 < nblk; b0 += 32) {
-        const int b = b0 + lane;
-        const bool mine = b < nblk;
-        uint32_t wv[16];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 q = nxt[i];
-            wv[4 * i + 0] = q.x;
-            wv[4 * i + 1] = q.y;
-            wv[4 * i + 2] = q.z;
-            wv[4 * i + 3] = q.w;
-        }
-        if (b + 32 < nblk) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) nxt[i] = __ldcs(reinterpret_cast<const uint4*>(row + (b + 32) * 32) + i);
-        }
-        float x[32];
-        uint32_t amax = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            x[2 * i] = __uint_as_float(wv[i] << 16);
-            x[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
-            amax = max(amax, __float_as_uint(x[2 * i]) & 0x7FFFFFFFu);
-            amax = max(amax, __float_as_uint(x[2 * i + 1]) & 0x7FFFFFFFu);
-        }
-        const int X = mx_e4m3_block_exponent(amax);
-        const float sc = exp2_neg(X);
-        uint32_t codes[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t lo = f32x2_to_e4m3x2_satfinite(x[4 * i] * sc, x[4 * i + 1] * sc);
-            const uint32_t hi = f32x2_to_e4m3x2_satfinite(x[4 * i + 2] * sc, x[4 * i + 3] * sc);
-            codes[i] = lo | (hi << 16);
-        }
-        const uint32_t sb = static_cast<uint32_t>(X + 127) & 0xFFu;
-        const bool full = b0 + 32 <= nblk;   // warp-uniform
-        if (full) {
-            // lane l stores bytes [16 l, 16 l + 16) and [512 + 16 l, ...) of the pass's
-            // 1 KB per row, taken from the owning lanes (l / 2 and 16 + l / 2, half l % 2)
-            const int src0 = lane >> 1, src1 = 16 + (lane >> 1);
-            const bool hi = lane & 1;
-            uint32_t w0[4], w1[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t lo0 = __shfl_sync(0xffffffffu, codes[i], src0);
-                const uint32_t hi0 = __shfl_sync(0xffffffffu, codes[4 + i], src0);
-                const uint32_t lo1 = __shfl_sync(0xffffffffu, codes[i], src1);
-                const uint32_t hi1 = __shfl_sync(0xffffffffu, codes[4 + i], src1);
-                w0[i] = hi ? hi0 : lo0;
-                w1[i] = hi ? hi1 : lo1;
-            }
-            const uint4 st0 = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-            const uint4 st1 = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-            // the scale bytes of blocks 4j..4j+3 packed into one word by lane 4j
-            uint32_t sword = sb;
-            sword |= __shfl_down_sync(0xffffffffu, sb, 1) << 8;
-            sword |= __shfl_down_sync(0xffffffffu, sb, 2) << 16;
-            sword |= __shfl_down_sync(0xffffffffu, sb, 3) << 24;
-            for (int j = 0; j < k; ++j) {
-                const int p = s_dst[wib][j];
-                if (p < 0) continue;
-                uint4* rowp = reinterpret_cast<uint4*>(a1 + static_cast<size_t>(p) * H + b0 * 32);
-                rowp[lane] = st0;
-                rowp[32 + lane] = st1;
-                if ((lane & 3) == 0)
-                    reinterpret_cast<uint32_t*>(a1_sf)[static_cast<size_t>(b >> 2) * S4 + p] = sword;
-            }
-        } else if (mine) {
-            for (int j = 0; j < k; ++j) {
-                const int p = s_dst[wib][j];
-                if (p < 0) continue;
-                uint4* dst = reinterpret_cast<uint4*>(a1 + static_cast<size_t>(p) * H + b * 32);
-                dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-                dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-                a1_sf[((static_cast<size_t>(b >> 2) * S4 + p) << 2) + (b & 3)] = static_cast<uint8_t>(sb);
-            }
-        }
-    }
+    quant_token_warp(hidden, t, H, k, inv_perm, a1, a1_sf, S4, s_dst[wib]);
 }
 
 cudaError_t launch_quant_scatter(const uint16_t* hidden, int T, int H, int k, const int32_t* inv_perm, uint8_t* a1,
@@ -160,53 +66,13 @@ cudaError_t launch_sf_to_kstep_major(const uint8_t* plain, int S, int K, uint8_t
     return cudaGetLastError();
 }
 
-// out[t, h] = bf16( sum_j y[t*k + j, h] ) over slots with a valid id, summed
-// in fp32 in slot order (y rows were already multiplied by topk_w).
+// out[t, h] = bf16( sum_j y[t*k + j, h] ) (combine_rows in kt_quant_dev.cuh).
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ ids,
                                                       int T, int H, int k, int E, uint16_t* __restrict__ out) {
     griddep_wait();
     griddep_launch_dependents();
-    const int h8n = H >> 3;
-    const long long n = static_cast<long long>(T) * h8n;
-    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
-         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int t = static_cast<int>(idx / h8n);
-        const int h8 = static_cast<int>(idx % h8n);
-        float acc[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        // slots in order (the sum order is fixed); loads of four slots are in flight together
-        for (int j0 = 0; j0 < k; j0 += 4) {
-            uint4 q[4];
-            bool use[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int j = j0 + u;
-                int e = -1;
-                if (j < k) e = __ldg(ids + static_cast<size_t>(t) * k + j);
-                use[u] = e >= 0 && e < E;
-                q[u] = use[u] ? __ldcs(reinterpret_cast<const uint4*>(y + (static_cast<size_t>(t) * k + j) * H + h8 * 8))
-                              : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (!use[u]) continue;
-                const uint32_t wv[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[2 * i] += __uint_as_float(wv[i] << 16);
-                    acc[2 * i + 1] += __uint_as_float(wv[i] & 0xFFFF0000u);
-                }
-            }
-        }
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-            o[i] = *reinterpret_cast<const uint32_t*>(&b2);
-        }
-        *reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H + h8 * 8) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
+    combine_rows<false>(y, ids, T, H, k, E, out, static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x,
+                        static_cast<long long>(gridDim.x) * blockDim.x);
 }
 
 cudaError_t launch_combine(const uint16_t* y, const int32_t* ids, int T, int H, int k, int E, uint16_t* out,

@@ -232,6 +232,17 @@ def test_chained_kernels_wait_before_touching_memory():
     chained.add("mx_gemm_kernel")   # launched with the attribute through cudaLaunchKernelEx
     bodies = _kernel_bodies(src)
     assert chained <= set(bodies), chained - set(bodies)
+    # the GEMM kernels delegate to gemm_body (shared with the single-launch decode kernel)
+    assert "gemm_body<MODE, 1>" in bodies["mx_gemm_kernel"]
+    m = re.search(r"void\s+gemm_body\s*\(", src)
+    start = src.index("{", m.end())
+    depth, i = 0, start
+    while True:
+        depth += {"{": 1, "}": -1}.get(src[i], 0)
+        if depth == 0:
+            break
+        i += 1
+    bodies["mx_gemm_kernel"] = src[start:i + 1]
     for name in sorted(chained):
         body = bodies[name]
         assert "griddep_wait();" in body, name
