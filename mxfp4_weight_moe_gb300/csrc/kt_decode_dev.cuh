@@ -18,27 +18,34 @@ namespace kt {
 
 // Route one token with one warp: k rounds of a warp arg-max over its E
 // logits (value descending, index ascending; lane l holds experts l, l+32,
-// ...), then the gating weights in fp64, rounded to f32 once: the softmax
-// over the k selected logits (renormalize) or the full softmax over E taken
-// at them.  Top-k routing as in the DeepSeek-V4-Flash (top-6 of 256) and
-// Kimi-K3 (top-16 of 896) layers the pages name.
-__device__ __forceinline__ void route_token_warp(const float* __restrict__ row, int E, int k, int renormalize,
-                                                 int32_t* __restrict__ ids, float* __restrict__ w) {
+// ... in EPL registers, EPL a power of two >= ceil(E / 32)), then the gating
+// weights in fp64, rounded to f32 once: the softmax over the k selected
+// logits (renormalize) or the full softmax over E taken at them.  Top-k
+// routing as in the DeepSeek-V4-Flash (top-6 of 256) and Kimi-K3 (top-16 of
+// 896) layers the pages name.
+template <int EPL>
+__device__ __forceinline__ void route_token_warp_t(const float* __restrict__ row, int E, int k, int renormalize,
+                                                   int32_t* __restrict__ ids, float* __restrict__ w) {
     const int lane = threadIdx.x & 31;
-    const int epl = (E + 31) >> 5;   // <= 32 for E <= 1024
     constexpr int kNone = 0x7fffffff;
+    float v[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = (e < E) ? __ldg(row + e) : -INFINITY;
+    }
     uint32_t taken = 0;
     int my_id = 0;
     float my_v = 0.f;
     for (int j = 0; j < k; ++j) {
         float bv = -INFINITY;
         int bi = kNone;
-        for (int i = 0; i < epl; ++i) {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
             if (e < E && !((taken >> i) & 1u)) {
-                const float v = __ldg(row + e);
-                if (bi == kNone || v > bv) {
-                    bv = v;
+                if (bi == kNone || v[i] > bv) {
+                    bv = v[i];
                     bi = e;
                 }
             }
@@ -65,14 +72,26 @@ __device__ __forceinline__ void route_token_warp(const float* __restrict__ row, 
     if (renormalize) {
         for (int jj = 0; jj < k; ++jj) part += __shfl_sync(0xffffffffu, ex, jj);
     } else {
-        for (int i = 0; i < epl; ++i) {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
-            if (e < E) part += exp(static_cast<double>(__ldg(row + e)) - lmax);
+            if (e < E) part += exp(static_cast<double>(v[i]) - lmax);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
     }
     if (lane < k) w[lane] = static_cast<float>(ex / part);
+}
+
+__device__ __forceinline__ void route_token_warp(const float* __restrict__ row, int E, int k, int renormalize,
+                                                 int32_t* __restrict__ ids, float* __restrict__ w) {
+    const int epl = (E + 31) >> 5;   // E <= 1024 keeps this <= 32
+    if (epl <= 1) route_token_warp_t<1>(row, E, k, renormalize, ids, w);
+    else if (epl <= 2) route_token_warp_t<2>(row, E, k, renormalize, ids, w);
+    else if (epl <= 4) route_token_warp_t<4>(row, E, k, renormalize, ids, w);
+    else if (epl <= 8) route_token_warp_t<8>(row, E, k, renormalize, ids, w);
+    else if (epl <= 16) route_token_warp_t<16>(row, E, k, renormalize, ids, w);
+    else route_token_warp_t<32>(row, E, k, renormalize, ids, w);
 }
 
 // Stable token-to-expert permutation of S <= kDecodeMaxSlots slots by one

@@ -678,8 +678,11 @@ __device__ __forceinline__ void gemm_body(const GemmMaps* M, const KParams* PP, 
         grid_barrier(d->grid_ctr, 2 * g, abort_flag, p.err, p.wait_limit_ns);
         if (!*abort_flag) {
             int* s_dst = reinterpret_cast<int*>(epi) + 64 + warp * kMaxTopK;
-            for (int t = gw; t < d->T; t += nwg)
-                quant_token_warp(d->hidden, t, d->H, d->k, d->inv_perm, d->a1, d->a1_sf, d->S4, s_dst);
+            const int per_row = quant_items_per_row(d->H);
+            for (int item = gw; item < d->T * per_row; item += nwg) {
+                const int t = item / per_row, c = item - (item / per_row) * per_row;
+                quant_token_warp(d->hidden, t, d->H, d->k, d->inv_perm, d->a1, d->a1_sf, d->S4, s_dst, c, c + 1);
+            }
         }
         grid_barrier(d->grid_ctr, 3 * g, abort_flag, p.err, p.wait_limit_ns);
         for (int i = threadIdx.x; i <= p.E; i += kThreads) s_cp[i] = __ldcg(d->chunk_prefix + i);
@@ -697,6 +700,12 @@ __device__ __forceinline__ void gemm_body(const GemmMaps* M, const KParams* PP, 
         P[i].fc1 = pass_fc1<MODE>(i);
     }
 
+    // Work units of pass i, from kernel parameter space (the producer, MMA and epilogue loops below unroll
+    // their pass loop, so PP[pass] resolves to a parameter at a fixed offset; the table P is only indexed
+    // at run time by the scale warps' cursor)
+    const int units_all = *abort_flag ? 0 : s_cp[p.E];
+    auto pass_total = [&](int i) { return PP[i].nfg * units_all; };
+
     if (warp == 0 || warp == 3) {
         // ------------------------------------------------------------ producers (one lane each)
         if (lane == 0) {
@@ -710,19 +719,23 @@ __device__ __forceinline__ void gemm_body(const GemmMaps* M, const KParams* PP, 
             const uint64_t pol_a = l2_policy_evict_last();
             RingProducer rp;
             long long gi = 0;
-            for (int pass = 0; pass < NP && ok; ++pass) {
-            const Pass& ps = P[pass];
-            const KParams& pp = *ps.p;
-            const GemmMaps& mm = *ps.m;
-            const int nq = ps.nq;
+#pragma unroll
+            for (int pass = 0; pass < NP; ++pass) {
+            if (!ok) break;
+            const KParams& pp = PP[pass];
+            const GemmMaps& mm = M[pass];
+            const bool fc1p = pass_fc1<MODE>(pass);
+            const bool inter = fc1p && pp.interleaved;
+            const int nq = pp.K / 128;
+            const int total = pass_total(pass);
             // FC2 token rows (A2) are written by every CTA's FC1 epilogue in this launch
             if (MODE == kFused && pass == 1 && !weights)
                 ok = wait_count(d->fc1_done, gridDim.x * 4u, abort_flag, p.err, p.wait_limit_ns);
-            for (int u = first; u < ps.total && ok; u += stride) {
+            for (int u = first; u < total && ok; u += stride) {
                 TileInfo ti;
                 decode_tile<MODE>(pp, tb, u, rank, ti);
                 int wy, wz;
-                weight_coords(ps.fc1, pp, ti, wy, wz);
+                weight_coords(fc1p, pp, ti, wy, wz);
                 const uint32_t need = stage_bytes(ti);
                 const int nk = (nq + ti.kqs - 1) / ti.kqs;
                 const int share = (ti.nmma >> 3) / cl;            // 8-row groups this CTA loads
@@ -744,9 +757,9 @@ __device__ __forceinline__ void gemm_body(const GemmMaps* M, const KParams* PP, 
                     if (weights) {
                         mbar_arrive_expect_tx(full_bar(slot), kQuadWTx * ti.kqs);
                         const CUtensorMap* wm = &mm.w[ti.kqs - 1];
-                        if (ps.fc1 && pp.interleaved)
+                        if (inter)
                             tma_load_5d_hint(dst, wm, full_bar(slot), 0, wy, 0, wz, kq0, pol_w);
-                        else if (ps.fc1)
+                        else if (fc1p)
                             tma_load_4d_hint(dst, wm, full_bar(slot), 0, wy, wz, kq0, pol_w);
                         else
                             tma_load_3d_hint(dst, wm, full_bar(slot), 0, wy, kq0, pol_w);
@@ -950,11 +963,14 @@ __device__ __forceinline__ void gemm_body(const GemmMaps* M, const KParams* PP, 
             // 32-byte K step of a quad adds 2.  The issuing lane runs alone, so its instruction
             // chain is kept short: no descriptor is rebuilt inside the stage loop.
             const uint64_t dA_t = sdesc_sw128_sbo(0u, 1024);
-            for (int pass = 0; pass < NP && ok; ++pass) {
-            const int nq = P[pass].nq;
-            for (int u = first; u < P[pass].total && ok; u += stride, ++it) {
+#pragma unroll
+            for (int pass = 0; pass < NP; ++pass) {
+            if (!ok) break;
+            const int nq = PP[pass].K / 128;
+            const int total = pass_total(pass);
+            for (int u = first; u < total && ok; u += stride, ++it) {
                 TileInfo ti;
-                decode_tile<MODE>(*P[pass].p, tb, u, rank, ti);
+                decode_tile<MODE>(PP[pass], tb, u, rank, ti);
                 const int ab = it & 1;
                 issued = true;
                 ok = wait(acc_empty(ab), ((acc_ph >> ab) & 1u) ^ 1u);
@@ -987,8 +1003,8 @@ __device__ __forceinline__ void gemm_body(const GemmMaps* M, const KParams* PP, 
                         auto issue_quad = [&](int q) {
                             const int kq = kq0 + q;
                             const uint32_t t_sfa = t_sf + static_cast<uint32_t>(kq & (kGroup - 1)) * kSfQuadCols;
-                            const uint64_t dA = dA_t + sa + static_cast<uint64_t>(q * (kQuadW >> 4));
                             const uint64_t dB = dB_t + sa + b_off16 + static_cast<uint64_t>(q * (1024 >> 4));
+                            const uint64_t dA = dA_t + sa + static_cast<uint64_t>(q * (kQuadW >> 4));
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 const uint32_t idesc =
@@ -1037,12 +1053,14 @@ __device__ __forceinline__ void gemm_body(const GemmMaps* M, const KParams* PP, 
         uint32_t acc_ph = 0u;                          // one parity bit per buffer
         int it = 0;
         bool ok = true;
+#pragma unroll
         for (int pass = 0; pass < NP; ++pass) {
-        const KParams& pp = *P[pass].p;
+        const KParams& pp = PP[pass];
         const int ek = MODE == kFused ? (pass == 0 ? static_cast<int>(GemmEpilogue::SwiGLU)
                                                    : static_cast<int>(GemmEpilogue::Combine))
                                       : MODE;
-        for (int u = first; u < P[pass].total && ok; u += stride, ++it) {
+        const int total = pass_total(pass);
+        for (int u = first; u < total && ok; u += stride, ++it) {
             TileInfo ti;
             decode_tile<MODE>(pp, tb, u, rank, ti);
             const int ab = it & 1;
@@ -1341,28 +1359,31 @@ static bool encode_maps(const GemmArgs& a, GemmMaps& maps) {
     const bool sfa_tma = (a.K % 512) == 0;
     bool ok = true;
     const bool inter = fc1 && a.interleaved;
+    // Weight tiles: with the A operand in tensor memory, packed bytes (64 per row per K quad) in the 64-byte
+    // swizzle the expanding warps read conflict-free; otherwise the unpacking type (one byte per element) in
+    // the 128-byte swizzle the MMA reads.  x counts bytes or elements accordingly.
+    const CUtensorMapDataType wt = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
+    const uint64_t wx = 128;
+    const CUtensorMapSwizzle wsw = CU_TENSOR_MAP_SWIZZLE_128B;
     for (int kq = 1; kq <= 2; ++kq) {
         if (inter) {
             // interleaved w13 viewed as [K/128 quad][E][2 parity][I][128]: row 2i + parity of expert e
-            const uint64_t dw[5] = {128, static_cast<uint64_t>(a.I), 2, static_cast<uint64_t>(a.E), K / 128};
+            const uint64_t dw[5] = {wx, static_cast<uint64_t>(a.I), 2, static_cast<uint64_t>(a.E), K / 128};
             const uint64_t sw[4] = {K, K / 2, static_cast<uint64_t>(a.I) * K, 64};
-            const uint32_t bw[5] = {128, 64, 2, 1, static_cast<uint32_t>(kq)};
-            ok = ok && encode(&maps.w[kq - 1], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.w, 5, dw, sw, bw,
-                              CU_TENSOR_MAP_SWIZZLE_128B);
+            const uint32_t bw[5] = {static_cast<uint32_t>(wx), 64, 2, 1, static_cast<uint32_t>(kq)};
+            ok = ok && encode(&maps.w[kq - 1], wt, a.w, 5, dw, sw, bw, wsw);
         } else if (fc1) {
             // w13 viewed as [K/128 quad][2E][I][128]: (z = 2e + gate/up, y = row within the half)
-            const uint64_t dw[4] = {128, static_cast<uint64_t>(a.I), 2ull * a.E, K / 128};
+            const uint64_t dw[4] = {wx, static_cast<uint64_t>(a.I), 2ull * a.E, K / 128};
             const uint64_t sw[3] = {K / 2, static_cast<uint64_t>(a.I) * (K / 2), 64};
-            const uint32_t bw[4] = {128, 64, 2, static_cast<uint32_t>(kq)};
-            ok = ok && encode(&maps.w[kq - 1], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.w, 4, dw, sw, bw,
-                              CU_TENSOR_MAP_SWIZZLE_128B);
+            const uint32_t bw[4] = {static_cast<uint32_t>(wx), 64, 2, static_cast<uint32_t>(kq)};
+            ok = ok && encode(&maps.w[kq - 1], wt, a.w, 4, dw, sw, bw, wsw);
         } else {
             // w viewed as [K/128 quad][E * rows_w][128]
-            const uint64_t dw[3] = {128, wrows, K / 128};
+            const uint64_t dw[3] = {wx, wrows, K / 128};
             const uint64_t sw[2] = {K / 2, 64};
-            const uint32_t bw[3] = {128, 128, static_cast<uint32_t>(kq)};
-            ok = ok && encode(&maps.w[kq - 1], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.w, 3, dw, sw, bw,
-                              CU_TENSOR_MAP_SWIZZLE_128B);
+            const uint32_t bw[3] = {static_cast<uint32_t>(wx), 128, static_cast<uint32_t>(kq)};
+            ok = ok && encode(&maps.w[kq - 1], wt, a.w, 3, dw, sw, bw, wsw);
         }
         // activations viewed as [S8/8 group][K/128 quad][8 rows][128]; rows up
         // to S8 = S rounded up to 8 must be addressable (callers pad the buffer)

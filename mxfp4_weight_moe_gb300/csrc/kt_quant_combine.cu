@@ -12,7 +12,7 @@
 
 namespace kt {
 
-// One warp per token row (quant_token_warp in kt_quant_dev.cuh).
+// One warp per (token row, pass of 1024 elements) (quant_token_warp in kt_quant_dev.cuh).
 __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __restrict__ hidden, int T, int H, int k,
                                                             const int32_t* __restrict__ inv_perm,
                                                             uint8_t* __restrict__ a1, uint8_t* __restrict__ a1_sf,
@@ -21,16 +21,20 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
     griddep_launch_dependents();
     __shared__ int s_dst[8][kMaxTopK];
     const int wib = threadIdx.x >> 5;
-    const int t = blockIdx.x * 8 + wib;
-    if (t >= T) return;   // whole warp
-    quant_token_warp(hidden, t, H, k, inv_perm, a1, a1_sf, S4, s_dst[wib]);
+    const int per_row = quant_items_per_row(H);
+    const long long item = static_cast<long long>(blockIdx.x) * 8 + wib;
+    if (item >= static_cast<long long>(T) * per_row) return;   // whole warp
+    const int t = static_cast<int>(item / per_row);
+    const int c = static_cast<int>(item - static_cast<long long>(t) * per_row);
+    quant_token_warp(hidden, t, H, k, inv_perm, a1, a1_sf, S4, s_dst[wib], c, c + 1);
 }
 
 cudaError_t launch_quant_scatter(const uint16_t* hidden, int T, int H, int k, const int32_t* inv_perm, uint8_t* a1,
                                  uint8_t* a1_sf, int S4, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    const cudaError_t e = launch_chained(quant_scatter_kernel, dim3((T + 7) / 8), dim3(256), 0, s, hidden, T, H, k,
-                                         inv_perm, a1, a1_sf, S4);
+    const long long items = static_cast<long long>(T) * quant_items_per_row(H);
+    const cudaError_t e = launch_chained(quant_scatter_kernel, dim3(static_cast<unsigned>((items + 7) / 8)), dim3(256),
+                                         0, s, hidden, T, H, k, inv_perm, a1, a1_sf, S4);
     count_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

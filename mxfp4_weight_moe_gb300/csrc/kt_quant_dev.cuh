@@ -14,29 +14,40 @@
 
 namespace kt {
 
-// Lane l quantises 32-element blocks l, l+32, ... (64 contiguous input bytes
-// each); the 32 codes + scale byte go to every permuted row the token's k
-// slots map to (inv_perm; a slot of -1 is skipped).  The codes of a pass of
-// 32 blocks (1 KB per row) are exchanged through shuffles once, so that each
-// store instruction writes 512 contiguous bytes of a row: one 16-byte store
-// per lane at a 32-byte stride left half-filled sectors and measured 25-33 %
-// slower on GB300.  s_dst: kMaxTopK ints of shared memory owned by the warp.
+// Passes of 32 blocks (1024 elements) of one token row that one warp-level
+// work item of the quantiser takes: a row of H elements is ceil(H / 1024)
+// items, so that decode-sized batches spread over many warps.
+constexpr int kQuantPass = 32;
+__host__ __device__ __forceinline__ int quant_items_per_row(int H) { return ((H >> 5) + kQuantPass - 1) / kQuantPass; }
+
+// Lane l quantises 32-element blocks b0 + l of the passes in [pass0, pass1)
+// (64 contiguous input bytes each); the 32 codes + scale byte go to every
+// permuted row the token's k slots map to (inv_perm; a slot of -1 is
+// skipped).  The codes of a pass of 32 blocks (1 KB per row) are exchanged
+// through shuffles once, so that each store instruction writes 512
+// contiguous bytes of a row: one 16-byte store per lane at a 32-byte stride
+// left half-filled sectors and measured 25-33 % slower on GB300.
+// s_dst: kMaxTopK ints of shared memory owned by the warp.
 __device__ __forceinline__ void quant_token_warp(const uint16_t* __restrict__ hidden, int t, int H, int k,
                                                  const int32_t* __restrict__ inv_perm, uint8_t* __restrict__ a1,
-                                                 uint8_t* __restrict__ a1_sf, int S4, int* s_dst) {
+                                                 uint8_t* __restrict__ a1_sf, int S4, int* s_dst, int pass0 = 0,
+                                                 int pass1 = 1 << 30) {
     const int lane = threadIdx.x & 31;
     if (lane < k) s_dst[lane] = __ldcg(inv_perm + static_cast<size_t>(t) * k + lane);
     __syncwarp();
-    const int nblk = H >> 5;
+    const int nblk_row = H >> 5;
+    const int bend = min(nblk_row, pass1 * kQuantPass);
+    const int nblk = bend;
     const uint16_t* row = hidden + static_cast<size_t>(t) * H;
     // warp-uniform passes of 32 blocks: lane l converts block b0 + l (if it
     // exists); the next pass's block is loaded before this one is converted
     uint4 nxt[4] = {};
-    if (lane < nblk) {
+    const int bstart = pass0 * kQuantPass;
+    if (bstart + lane < nblk) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) nxt[i] = __ldcs(reinterpret_cast<const uint4*>(row + lane * 32) + i);
+        for (int i = 0; i < 4; ++i) nxt[i] = __ldcs(reinterpret_cast<const uint4*>(row + (bstart + lane) * 32) + i);
     }
-    for (int b0 = 0; b0 < nblk; b0 += 32) {
+    for (int b0 = bstart; b0 < nblk; b0 += 32) {
         const int b = b0 + lane;
         const bool mine = b < nblk;
         uint32_t wv[16];
