@@ -22,8 +22,9 @@ namespace kt {
 // weights in fp64, rounded to f32 once: the softmax over the k selected
 // logits (renormalize) or the full softmax over E taken at them.  Top-k
 // routing as in the DeepSeek-V4-Flash (top-6 of 256) and Kimi-K3 (top-16 of
-// 896) layers the pages name.
-template <int EPL>
+// 896) layers the pages name.  kShared: the logits row (and nothing else)
+// is in shared memory.
+template <int EPL, bool kShared>
 __device__ __forceinline__ void route_token_warp_t(const float* __restrict__ row, int E, int k, int renormalize,
                                                    int32_t* __restrict__ ids, float* __restrict__ w) {
     const int lane = threadIdx.x & 31;
@@ -32,7 +33,7 @@ __device__ __forceinline__ void route_token_warp_t(const float* __restrict__ row
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
-        v[i] = (e < E) ? __ldg(row + e) : -INFINITY;
+        v[i] = (e < E) ? (kShared ? row[e] : __ldg(row + e)) : -INFINITY;
     }
     uint32_t taken = 0;
     int my_id = 0;
@@ -83,15 +84,16 @@ __device__ __forceinline__ void route_token_warp_t(const float* __restrict__ row
     if (lane < k) w[lane] = static_cast<float>(ex / part);
 }
 
+template <bool kShared = false>
 __device__ __forceinline__ void route_token_warp(const float* __restrict__ row, int E, int k, int renormalize,
                                                  int32_t* __restrict__ ids, float* __restrict__ w) {
     const int epl = (E + 31) >> 5;   // E <= 1024 keeps this <= 32
-    if (epl <= 1) route_token_warp_t<1>(row, E, k, renormalize, ids, w);
-    else if (epl <= 2) route_token_warp_t<2>(row, E, k, renormalize, ids, w);
-    else if (epl <= 4) route_token_warp_t<4>(row, E, k, renormalize, ids, w);
-    else if (epl <= 8) route_token_warp_t<8>(row, E, k, renormalize, ids, w);
-    else if (epl <= 16) route_token_warp_t<16>(row, E, k, renormalize, ids, w);
-    else route_token_warp_t<32>(row, E, k, renormalize, ids, w);
+    if (epl <= 1) route_token_warp_t<1, kShared>(row, E, k, renormalize, ids, w);
+    else if (epl <= 2) route_token_warp_t<2, kShared>(row, E, k, renormalize, ids, w);
+    else if (epl <= 4) route_token_warp_t<4, kShared>(row, E, k, renormalize, ids, w);
+    else if (epl <= 8) route_token_warp_t<8, kShared>(row, E, k, renormalize, ids, w);
+    else if (epl <= 16) route_token_warp_t<16, kShared>(row, E, k, renormalize, ids, w);
+    else route_token_warp_t<32, kShared>(row, E, k, renormalize, ids, w);
 }
 
 // Stable token-to-expert permutation of S <= kDecodeMaxSlots slots by one
@@ -103,6 +105,8 @@ __device__ __forceinline__ void route_token_warp(const float* __restrict__ row, 
 // warp finally sweeps its slots again in slot order and ranks equal experts
 // with match.any.  Writes expert_offsets [E+1], chunk_prefix [E+1], perm [S]
 // (-1 past the valid rows), inv_perm [S] (-1 for an id outside [0, E)).
+// kShared: ids and the four outputs are in shared memory (otherwise ids were
+// written earlier in the same launch and are read past L1).
 constexpr int kDecodeMaxSlots = KT_DECODE_MAX_SLOTS;
 
 __device__ __forceinline__ int block_exclusive_scan(int x, int* s_warp, int* total) {
@@ -134,6 +138,7 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int* s_warp, int* tot
     return res;
 }
 
+template <bool kShared = false>
 __device__ __forceinline__ void permute_block(const int32_t* __restrict__ ids, int S, int E,
                                               int32_t* __restrict__ offsets, int32_t* __restrict__ chunk_prefix,
                                               int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm, int* err,
@@ -151,7 +156,7 @@ __device__ __forceinline__ void permute_block(const int32_t* __restrict__ ids, i
         const int s = r + lane;
         int e = -1;
         if (s < s1) {
-            e = __ldcg(ids + s);   // written earlier in the same launch
+            e = kShared ? ids[s] : __ldcg(ids + s);   // written earlier in the same launch
             if (e < 0 || e >= E) {
                 bad = true;
                 e = -1;
@@ -205,7 +210,7 @@ __device__ __forceinline__ void permute_block(const int32_t* __restrict__ ids, i
         const int s = r + lane;
         int e = -1;
         if (s < s1) {
-            e = __ldcg(ids + s);
+            e = kShared ? ids[s] : __ldcg(ids + s);
             if (e < 0 || e >= E) e = -1;
         }
         const unsigned peers = __match_any_sync(0xffffffffu, e);

@@ -27,13 +27,18 @@ __host__ __device__ __forceinline__ int quant_items_per_row(int H) { return ((H 
 // through shuffles once, so that each store instruction writes 512
 // contiguous bytes of a row: one 16-byte store per lane at a 32-byte stride
 // left half-filled sectors and measured 25-33 % slower on GB300.
-// s_dst: kMaxTopK ints of shared memory owned by the warp.
+// s_dst: kMaxTopK ints of shared memory owned by the warp.  kSharedInv:
+// inv_perm is in shared memory (otherwise it was written earlier in the same
+// launch, or by an earlier kernel, and is read past L1).
+template <bool kSharedInv = false>
 __device__ __forceinline__ void quant_token_warp(const uint16_t* __restrict__ hidden, int t, int H, int k,
                                                  const int32_t* __restrict__ inv_perm, uint8_t* __restrict__ a1,
                                                  uint8_t* __restrict__ a1_sf, int S4, int* s_dst, int pass0 = 0,
                                                  int pass1 = 1 << 30) {
     const int lane = threadIdx.x & 31;
-    if (lane < k) s_dst[lane] = __ldcg(inv_perm + static_cast<size_t>(t) * k + lane);
+    if (lane < k)
+        s_dst[lane] = kSharedInv ? inv_perm[static_cast<size_t>(t) * k + lane]
+                                 : __ldcg(inv_perm + static_cast<size_t>(t) * k + lane);
     __syncwarp();
     const int nblk_row = H >> 5;
     const int bend = min(nblk_row, pass1 * kQuantPass);

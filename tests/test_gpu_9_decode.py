@@ -74,6 +74,11 @@ def test_decode_small_configs(name):
     (24, 512, 3, 3, 256, "normal"),      # k = E
     (64, 1024, 32, 32, 512, "uniform"),  # 2048 slots: the decode kernel's largest batch
     (3, 1024, 1024, 8, 256, "normal"),   # E = 1024: most experts idle
+    # above 4 tokens (or 16384 logits) routing runs as a warp per token across the grid and the
+    # permutation in CTA 0, with grid barriers between; smaller batches route and permute in every CTA
+    (64, 256, 512, 8, 128, "normal"),
+    (4, 256, 1024, 8, 128, "normal"),     # 4 tokens over 1024 experts: in every CTA
+    (128, 512, 256, 16, 256, "uniform"),  # 2048 slots on that path
 ])
 def test_decode_ragged_shapes(shape):
     T, H, E, k, I, recipe = shape
