@@ -59,14 +59,21 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// One bounded try_wait: the thread may suspend until the phase completes, for
+// at most kMbarSuspendNs.  Measured on GB300: without the hint (a system-
+// dependent suspend limit) the GEMM's stage loop ran 7 % slower on the
+// Kimi-K3-shaped and DeepSeek-V4-shaped layers than with any hint from 16 to
+// 256 ns, so a waiter evidently does not always resume as soon as the TMA
+// bytes or the tcgen05.commit land.
+constexpr uint32_t kMbarSuspendNs = 64;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred P1;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2, %3;\n\t"
         "selp.b32 %0, 1, 0, P1;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(kMbarSuspendNs)
         : "memory");
     return ok != 0;
 }
