@@ -421,20 +421,8 @@ __device__ __forceinline__ uint64_t sdesc_sw128_sbo(uint32_t saddr, uint32_t sbo
 }
 
 // Placement of stages in the ring: a stage of `need` bytes starts at the
-// head, or at the ring start if it would cross the end.  Offsets are virtual
-// (monotonic); the ring offset is start % kRing.
-struct StageRing {
-    uint64_t head = 0;
-    __device__ __forceinline__ uint64_t place(uint32_t need) {
-        const uint64_t phys = head % kRing;
-        if (phys + need > kRing) head += kRing - phys;
-        const uint64_t start = head;
-        head += need;
-        return start;
-    }
-};
-
-// The consumer's view of the same placement: only the ring offset.
+// head, or at the ring start if it would cross the end.  This is the
+// consumer's view (the ring offset only); RingProducer places identically.
 struct PhysRing {
     uint32_t phys = 0;
     __device__ __forceinline__ uint32_t place(uint32_t need) {
@@ -445,47 +433,69 @@ struct PhysRing {
     }
 };
 
-// Producer-side bookkeeping of the ring: stage gi's bytes end at
-// end_of(gi % kSlots); bytes before `tail` are free; stages below `released`
-// have completed.  Both producer threads run the same stage sequence and so
-// agree on every placement.  acquire() returns the stage's virtual start
-// once its barrier slot and its ring bytes are free, or ~0 on timeout.
+// Producer-side bookkeeping of the ring: stage gi (counted in `gi`) uses
+// barrier slot `slot` in lap `lap` (gi % kSlots and gi / kSlots, kept
+// incrementally), its bytes end at virtual offset end_of(slot), bytes before
+// `tail` are free and stages below `released` have completed.  Both producer
+// threads run the same stage sequence and so agree on every placement, and
+// the MMA warp's PhysRing reproduces the physical offsets.  The issuing
+// thread is alone on its warp's critical path, so the placement does no
+// 64-bit division per stage.
 struct RingProducer {
-    StageRing ring;
-    uint64_t b_end0 = 0, b_end1 = 0, b_end2 = 0, b_end3 = 0;   // registers, not a local array
+    uint64_t head = 0;    // virtual end of the last placed stage
+    uint32_t phys = 0;    // head % kRing
+    uint64_t b_end0 = 0, b_end1 = 0, b_end2 = 0, b_end3 = 0, b_end4 = 0;   // registers, not a local array
     uint64_t tail = 0;
-    long long released = 0;
-    static_assert(kSlots == 4, "one end offset per slot");
+    long long gi = 0, released = 0;
+    int slot = 0;
+    uint32_t lap = 0;
+    static_assert(kSlots <= 5, "one end offset per slot");
     __device__ __forceinline__ uint64_t end_of(int s) const {
-        return s == 0 ? b_end0 : s == 1 ? b_end1 : s == 2 ? b_end2 : b_end3;
+        return s == 0 ? b_end0 : s == 1 ? b_end1 : s == 2 ? b_end2 : s == 3 ? b_end3 : b_end4;
     }
     __device__ __forceinline__ void set_end(int s, uint64_t v) {
         if (s == 0) b_end0 = v;
         else if (s == 1) b_end1 = v;
         else if (s == 2) b_end2 = v;
-        else b_end3 = v;
+        else if (s == 3) b_end3 = v;
+        else b_end4 = v;
     }
-    __device__ __forceinline__ uint64_t acquire(long long gi, uint32_t need, uint32_t empty_base,
-                                                const volatile int* abort_flag, uint64_t limit) {
-        const int slot = static_cast<int>(gi % kSlots);
-        const uint32_t par = static_cast<uint32_t>((gi / kSlots) & 1) ^ 1u;
-        if (!mbar_wait(empty_base + 8u * slot, par, abort_flag, limit)) return ~0ull;
+    // Waits until stage gi's barrier slot and ring bytes are free, then places it: `off` is its
+    // offset in the ring and `s` its barrier slot, and the next call places stage gi + 1.  Returns
+    // false on timeout (or abort).
+    __device__ __forceinline__ bool acquire(uint32_t need, uint32_t empty_base, const volatile int* abort_flag,
+                                            uint64_t limit, uint32_t& off, int& s) {
+        if (!mbar_wait(empty_base + 8u * slot, (lap & 1u) ^ 1u, abort_flag, limit)) return false;
         if (gi >= kSlots) {   // stage gi - kSlots (and every earlier one) is done
             tail = end_of(slot);
             if (released < gi - kSlots + 1) released = gi - kSlots + 1;
         }
-        const uint64_t start = ring.place(need);
+        uint64_t start = head;
+        uint32_t p = phys;
+        if (p + need > static_cast<uint32_t>(kRing)) {   // a stage never wraps: start the next lap
+            start += kRing - p;
+            p = 0;
+        }
         while (start + need - tail > static_cast<uint64_t>(kRing)) {
-            // wait for the oldest stage still holding ring bytes
+            // wait for the oldest stage still holding ring bytes (the rare path: mixed stage sizes)
             const long long j = released;
             const int js = static_cast<int>(j % kSlots);
             if (!mbar_wait(empty_base + 8u * js, static_cast<uint32_t>((j / kSlots) & 1), abort_flag, limit))
-                return ~0ull;
+                return false;
             tail = end_of(js);
             released = j + 1;
         }
-        set_end(slot, start + need);
-        return start;
+        head = start + need;
+        phys = p + need;
+        set_end(slot, head);
+        off = p;
+        s = slot;
+        if (++slot == kSlots) {
+            slot = 0;
+            ++lap;
+        }
+        ++gi;
+        return true;
     }
 };
 
@@ -808,7 +818,6 @@ __device__ __forceinline__ void gemm_body(const GemmMaps* M, const KParams* PP, 
             const uint64_t pol_w = l2_policy_evict_normal();
             const uint64_t pol_a = l2_policy_evict_last();
             RingProducer rp;
-            long long gi = 0;
 #pragma unroll
             for (int pass = 0; pass < NP; ++pass) {
             if (!ok) break;
@@ -832,17 +841,17 @@ __device__ __forceinline__ void gemm_body(const GemmMaps* M, const KParams* PP, 
                 const int g0 = (ti.r_al >> 3) + rank * share;
                 const uint32_t gstride = static_cast<uint32_t>(ti.kqs) * 1024u;   // bytes per 8-row group
                 const CUtensorMap* tm = &mm.t[ti.kqs - 1][share - 1];   // one box covers this CTA's share
-                for (int kb = 0; kb < nk; ++kb, ++gi) {
-                    const uint64_t start = rp.acquire(gi, need, empty_base, abort_flag, p.wait_limit_ns);
-                    if (start == ~0ull) {
+                for (int kb = 0; kb < nk; ++kb) {
+                    uint32_t off;
+                    int slot;
+                    if (!rp.acquire(need, empty_base, abort_flag, p.wait_limit_ns, off, slot)) {
                         ok = false;
                         break;
                     }
-                    const int slot = static_cast<int>(gi % kSlots);
                     const bool withhold =
                         (p.debug_flags & KT_DEBUG_WITHHOLD_STAGE) && pass == 0 && u == first && kb == 0;
                     if (withhold) continue;   // test hook: a withheld stage is neither loaded nor signalled
-                    const uint32_t dst = ring_base + static_cast<uint32_t>(start % kRing);
+                    const uint32_t dst = ring_base + off;
                     const int kq0 = kb * ti.kqs;
                     if (weights) {
                         mbar_arrive_expect_tx(full_bar(slot), kQuadWTx * ti.kqs);
