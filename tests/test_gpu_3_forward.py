@@ -123,6 +123,9 @@ def test_forward_decode_shapes(shape):
     (600, 256, 4, 1, 128),     # ~150 tokens per expert: token chunks, odd tails
     (300, 128, 3, 3, 256),     # k = E, every expert gets every token (2 chunks of 150)
     (129, 256, 8, 2, 512),
+    # prefill-sized: ~267 rows per expert in two chunks, one-quad stages in 2-CTA clusters
+    (400, 384, 3, 2, 640),     # FC1 with K = 3 quads; FC2 (3 feature tiles) unclustered
+    (400, 512, 3, 2, 640),     # FC2 clustered with K = 5 quads
 ])
 def test_forward_ragged_shapes(shape):
     T, H, E, k, I = shape

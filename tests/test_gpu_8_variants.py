@@ -75,6 +75,7 @@ def _check(hidden, ids_np, w_np, W, tokens, **opts):
     (32, 1024, 16, 4, 512, "hot_cold"),     # small_T32: K % 512 == 0, scales by TMA
     (25, 384, 2, 2, 640, "normal"),         # ragged: K = 3 quads, scales by cp.async gathers
     (1, 128, 2, 2, 128, "normal"),          # the tiny layer
+    (256, 512, 4, 2, 256, "normal"),        # 128 rows per expert: prefill-sized tiles in 2-CTA clusters
 ])
 def test_variant_against_oracle(gate_up, activation, limit, shape):
     T, H, E, k, I, recipe = shape
