@@ -59,7 +59,7 @@ FP8_OVER_BF16 = 2.0     # nominal dense ratio (4.5 / 2.25 PFLOP/s); mxf8f6f4 run
 # traffic null.
 GEMM_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mxfp4_weight_moe_gb300", "csrc", "kt_gemm_mx.cu")
 FC1_TRAFFIC = {
-    ("dsv4", "d24202785e1bedaa3b238f9315d0a8d921266b5d928636db0d1eb5247ac0ed09"): 2747439360 + 47791360,
+    ("dsv4", "802e24481ce9e8648fbedcc657186c9d7e68dba60ee44dc9605cce4a4c0edd53"): 2460472064 + 52114688,
 }
 
 
