@@ -60,6 +60,7 @@ FP8_OVER_BF16 = 2.0     # nominal dense ratio (4.5 / 2.25 PFLOP/s); mxf8f6f4 run
 GEMM_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mxfp4_weight_moe_gb300", "csrc", "kt_gemm_mx.cu")
 FC1_TRAFFIC = {
     ("dsv4", "802e24481ce9e8648fbedcc657186c9d7e68dba60ee44dc9605cce4a4c0edd53"): 2460472064 + 52114688,
+    ("kimi_T8192", "802e24481ce9e8648fbedcc657186c9d7e68dba60ee44dc9605cce4a4c0edd53"): 28962077440 + 486142720,
 }
 
 
