@@ -5,8 +5,10 @@ fraction of the block-scaled roofline.
 One step = one pass of the layer's hot path over one batch: top-k routing
 from router logits, permutation, MXFP8 activation quantisation, FC1 +
 SwiGLU + requant, FC2 + combine (``kt_moe_route_permute`` then
-``kt_mxfp4_moe_forward``).  Inputs are seeded and synthetic, resident in HBM
-when the timed region starts; ``e2e`` repeats the measurement with the
+``kt_mxfp4_moe_forward_routed``, which reuses the routing call's
+permutation; decode-sized layers: ``kt_mxfp4_moe_decode``, one launch).
+Inputs are seeded and synthetic, resident in HBM when the timed region
+starts; ``e2e`` repeats the measurement with the
 step's inputs (hidden, logits) copied from pinned host memory and the output
 copied back inside the timed region.
 
@@ -352,7 +354,7 @@ def run_ours(args, cfg, full: bool = True):
     stream = torch.cuda.current_stream(dev)
 
     # Decode-sized batches of small layers run as ONE launch (routing, permutation and the layer forward),
-    # where the seven launches' latency is most of the step.  Where the step streams gigabytes of experts
+    # where the separate launches' latency is most of the step.  Where the step streams gigabytes of experts
     # (the Kimi-K3-shaped layer at T=16: 9 GB) launch latency is noise, and the separate GEMM launches
     # measured faster than the single launch's GEMM passes; auto keeps those on the multi-launch path.
     layer_weight_bytes = E * (2 * I * H // 2 + 2 * I * H // 32 + H * I // 2 + H * I // 32)
@@ -363,8 +365,8 @@ def run_ours(args, cfg, full: bool = True):
         if use_decode:
             kt.decode(lg, h, k, *W, out=o, topk=route_out[:2], workspace=ws, stream=s)
         else:
-            ids, w, *_ = kt.route_permute(lg, k, out=route_out, workspace=ws_route, stream=s)
-            kt.forward(h, ids, w, *W, out=o, workspace=ws, stream=s)
+            ids, w, offs, perm, inv = kt.route_permute(lg, k, out=route_out, workspace=ws_route, stream=s)
+            kt.forward(h, ids, w, *W, out=o, workspace=ws, stream=s, routing=(offs, perm, inv))
 
     for _ in range(args.warmup):
         step()
@@ -513,7 +515,7 @@ def run_ours(args, cfg, full: bool = True):
                      "peak_source": f"{peak_src} hbm_gbs",
                      "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": fc1_ms},
         "path": "decode: one launch (route, permute, quantise, FC1, FC2, combine)" if use_decode
-        else "route_permute + forward (7 launches)",
+        else "route_permute + forward_routed (separate launches)",
         "layer_roofline": {"t_roof_ms": t_roof_ms, "frac": t_roof_ms / ms_per_step,
                            "bytes": work["layer_bytes"], "flops": work["layer_flops"],
                            "hbm_gbs": hbm, "mx_tflops": mx_tflops,

@@ -231,11 +231,32 @@ kt_status kt_mxfp4_moe_forward_ex(const uint16_t* hidden, int T, int H,
                                   const kt_moe_options* opts, void* stream);
 
 /*
+ * kt_mxfp4_moe_forward_ex on a routing that kt_moe_route_permute (or
+ * kt_moe_route_permute_noalloc) has already permuted: expert_offsets [E+1],
+ * perm [S] and inv_perm [S] (S = T * k; device pointers, 16-byte aligned)
+ * are that call's outputs for the same topk_ids and are used as they are,
+ * so the forward skips its own histogram -> scan -> scatter (three launches;
+ * one small launch derives the per-expert chunk counts instead).  Results
+ * are bit-identical to kt_mxfp4_moe_forward_ex.  The arrays must be exactly
+ * those outputs: the GEMMs take row ranges from them without re-checking.
+ * Other arguments, limits, ownership and errors as kt_mxfp4_moe_forward_ex;
+ * a NULL routing array is KT_ERR_INVALID_ARG.
+ */
+kt_status kt_mxfp4_moe_forward_routed(const uint16_t* hidden, int T, int H,
+                                      const int32_t* topk_ids, const float* topk_w, int k,
+                                      const int32_t* expert_offsets, const int32_t* perm,
+                                      const int32_t* inv_perm,
+                                      const uint8_t* w13, const uint8_t* w13_sf,
+                                      const uint8_t* w2, const uint8_t* w2_sf, int E, int I,
+                                      uint16_t* out, void* ws, size_t ws_bytes,
+                                      const kt_moe_options* opts, void* stream);
+
+/*
  * Single-launch decode: routing, permutation and the layer forward in ONE
  * kernel launch, for decode-sized batches (T * k <= KT_DECODE_MAX_SLOTS).
  * It computes exactly what kt_moe_route_permute followed by
  * kt_mxfp4_moe_forward_ex compute (same ids, weights, permutation and
- * kernels' arithmetic), without their seven launches: one cooperative kernel
+ * kernels' arithmetic), without their separate launches: one cooperative kernel
  * with one CTA per SM runs route -> permute -> MXFP8 quantisation -> FC1 +
  * SwiGLU -> FC2 -> combine, with grid-wide barriers (each wait bounded by the
  * same deadline as the GEMM barriers; an expired wait sets

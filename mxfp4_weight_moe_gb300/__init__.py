@@ -68,6 +68,8 @@ _SIGNATURES = {
     "kt_mxfp4_moe_forward": ([_VP, _I, _I, _VP, _VP, _I, _VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _SZ, _VP], _I),
     "kt_mxfp4_moe_forward_ex": ([_VP, _I, _I, _VP, _VP, _I, _VP, _VP, _VP, _VP, _I, _I, _VP, _VP, _SZ,
                                  ctypes.POINTER(MoeOptions), _VP], _I),
+    "kt_mxfp4_moe_forward_routed": ([_VP, _I, _I, _VP, _VP, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _VP,
+                                     _VP, _SZ, ctypes.POINTER(MoeOptions), _VP], _I),
     "kt_mxfp4_moe_decode": ([_VP, _VP, _I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
                              ctypes.POINTER(MoeOptions), _VP], _I),
     "kt_moe_workspace_layout": ([_I, _I, _I, _I, _I, ctypes.POINTER(WsLayout)], _I),
@@ -249,13 +251,16 @@ def route_permute(logits: torch.Tensor, k: int, renormalize: bool = True, stream
 def forward(hidden: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, w13: torch.Tensor,
             w13_sf: torch.Tensor, w2: torch.Tensor, w2_sf: torch.Tensor, out: torch.Tensor | None = None,
             workspace: torch.Tensor | None = None, stream=None, gate_up: str = "halves",
-            activation: str = "swiglu", alpha: float = 1.702, limit: float = 7.0) -> torch.Tensor:
+            activation: str = "swiglu", alpha: float = 1.702, limit: float = 7.0,
+            routing: tuple | None = None) -> torch.Tensor:
     """One fused MoE layer forward; returns out (bf16 [T, H]).
 
     gate_up "halves" (w13 rows [0, I) gate, [I, 2I) up) or "interleaved"
     (row 2i gate i, row 2i+1 up i); activation "swiglu" (silu(g) * u) or
     "swiglu_clamped" (the clamped SwiGLU of GPT-OSS-format checkpoints, with
-    alpha and limit; see kt_moe_options in kt_moe.h)."""
+    alpha and limit; see kt_moe_options in kt_moe.h).  routing: the
+    (expert_offsets, perm, inv_perm) that route_permute returned for these
+    topk_ids, reused instead of re-derived (kt_mxfp4_moe_forward_routed)."""
     _need(hidden, "hidden", torch.bfloat16, 2)
     dev = hidden.device
     _need(topk_ids, "topk_ids", torch.int32, 2, dev)
@@ -274,6 +279,24 @@ def forward(hidden: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, 
     _need(out, "out", torch.bfloat16, 2, dev)
     if workspace is None:   # a caller's workspace is size-checked by the library
         workspace = torch.empty(max(workspace_bytes(T, H, I, E, k), 1), dtype=torch.uint8, device=dev)
+    if routing is not None:
+        offsets, perm, inv_perm = routing
+        _need(offsets, "expert_offsets", torch.int32, 1, dev)
+        _need(perm, "perm", torch.int32, 1, dev)
+        _need(inv_perm, "inv_perm", torch.int32, 1, dev)
+        if offsets.numel() != E + 1 or perm.numel() != T * k or inv_perm.numel() != T * k:
+            raise ValueError("routing must be (expert_offsets [E+1], perm [T*k], inv_perm [T*k])")
+        if gate_up not in GATE_UP_LAYOUTS or activation not in ACTIVATIONS:
+            raise ValueError(f"gate_up must be one of {GATE_UP_LAYOUTS} and activation one of {ACTIVATIONS}")
+        opts = MoeOptions(GATE_UP_LAYOUTS.index(gate_up), ACTIVATIONS.index(activation), float(alpha), float(limit))
+        with _on_device(dev):
+            _check(lib().kt_mxfp4_moe_forward_routed(_ptr(hidden), T, H, _ptr(topk_ids), _ptr(topk_w), k,
+                                                     _ptr(offsets), _ptr(perm), _ptr(inv_perm), _ptr(w13),
+                                                     _ptr(w13_sf), _ptr(w2), _ptr(w2_sf), E, I, _ptr(out),
+                                                     _ptr(workspace), workspace.numel(), ctypes.byref(opts),
+                                                     _stream_ptr(stream, dev)),
+                   "kt_mxfp4_moe_forward_routed")
+        return out
     if gate_up == "halves" and activation == "swiglu":
         with _on_device(dev):
             _check(lib().kt_mxfp4_moe_forward(_ptr(hidden), T, H, _ptr(topk_ids), _ptr(topk_w), k, _ptr(w13),

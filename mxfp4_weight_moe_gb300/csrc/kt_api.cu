@@ -193,10 +193,14 @@ kt_status kt_mxfp4_moe_forward(const uint16_t* hidden, int T, int H, const int32
                                    nullptr, stream);
 }
 
-kt_status kt_mxfp4_moe_forward_ex(const uint16_t* hidden, int T, int H, const int32_t* topk_ids,
-                                  const float* topk_w, int k, const uint8_t* w13, const uint8_t* w13_sf,
-                                  const uint8_t* w2, const uint8_t* w2_sf, int E, int I, uint16_t* out, void* ws,
-                                  size_t ws_bytes, const kt_moe_options* opts, void* stream) {
+// The forward behind kt_mxfp4_moe_forward_ex (routed == false: the permutation is derived here from
+// topk_ids) and kt_mxfp4_moe_forward_routed (routed == true: r_offsets / r_perm / r_inv_perm are the
+// routing call's outputs).
+static kt_status forward_impl(const uint16_t* hidden, int T, int H, const int32_t* topk_ids, const float* topk_w,
+                              int k, bool routed, const int32_t* r_offsets, const int32_t* r_perm,
+                              const int32_t* r_inv_perm, const uint8_t* w13, const uint8_t* w13_sf,
+                              const uint8_t* w2, const uint8_t* w2_sf, int E, int I, uint16_t* out, void* ws,
+                              size_t ws_bytes, const kt_moe_options* opts, void* stream) {
     g_last_error[0] = '\0';
     kt_moe_options o{KT_GATE_UP_HALVES, KT_ACT_SWIGLU, 1.0f, 0.0f};
     if (opts) o = *opts;
@@ -217,8 +221,12 @@ kt_status kt_mxfp4_moe_forward_ex(const uint16_t* hidden, int T, int H, const in
     if (T == 0) return KT_OK;
     if (!hidden || !topk_ids || !topk_w || !w13 || !w13_sf || !w2 || !w2_sf || !out || !ws)
         return fail(KT_ERR_INVALID_ARG, "null pointer argument");
+    if (routed && (!r_offsets || !r_perm || !r_inv_perm))
+        return fail(KT_ERR_INVALID_ARG, "null routing array (expert_offsets, perm, inv_perm)");
     if (!aligned(hidden, 16) || !aligned(out, 16) || !aligned(topk_ids, 16) || !aligned(topk_w, 16))
         return fail(KT_ERR_ALIGNMENT, "hidden, out, topk_ids and topk_w must be 16-byte aligned");
+    if (routed && (!aligned(r_offsets, 16) || !aligned(r_perm, 16) || !aligned(r_inv_perm, 16)))
+        return fail(KT_ERR_ALIGNMENT, "expert_offsets, perm and inv_perm must be 16-byte aligned");
     if (!aligned(w13, 32) || !aligned(w2, 32))
         return fail(KT_ERR_ALIGNMENT, "w13 and w2 must be 32-byte aligned");
     if (!aligned(w13_sf, 16) || !aligned(w2_sf, 16))
@@ -231,10 +239,10 @@ kt_status kt_mxfp4_moe_forward_ex(const uint16_t* hidden, int T, int H, const in
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* base = static_cast<uint8_t*>(ws);
     int* err = reinterpret_cast<int*>(base + L.err);
-    int32_t* offsets = reinterpret_cast<int32_t*>(base + L.expert_offsets);
+    const int32_t* offsets = routed ? r_offsets : reinterpret_cast<int32_t*>(base + L.expert_offsets);
     int32_t* chunk_prefix = reinterpret_cast<int32_t*>(base + L.chunk_prefix);
-    int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
-    int32_t* inv_perm = reinterpret_cast<int32_t*>(base + L.inv_perm);
+    const int32_t* perm = routed ? r_perm : reinterpret_cast<int32_t*>(base + L.perm);
+    const int32_t* inv_perm = routed ? r_inv_perm : reinterpret_cast<int32_t*>(base + L.inv_perm);
     uint8_t* a1 = base + L.a1;
     uint8_t* a1_sf = base + L.a1_sf;
     uint8_t* a2 = base + L.a2;
@@ -245,9 +253,14 @@ kt_status kt_mxfp4_moe_forward_ex(const uint16_t* hidden, int T, int H, const in
     if ((st = cuda_status(cudaMemsetAsync(err, 0, sizeof(int), s))) != KT_OK) return st;
     {
         StageTimer timer(KT_STAGE_PERMUTE, s);
-        if ((st = cuda_status(launch_permute(topk_ids, S, E, reinterpret_cast<int32_t*>(base + L.hist), offsets,
-                                             chunk_prefix, perm, inv_perm, err, s))) != KT_OK)
-            return st;
+        if (routed)
+            st = cuda_status(launch_chunk_prefix(offsets, E, chunk_prefix, s));
+        else
+            st = cuda_status(launch_permute(topk_ids, S, E, reinterpret_cast<int32_t*>(base + L.hist),
+                                            reinterpret_cast<int32_t*>(base + L.expert_offsets), chunk_prefix,
+                                            reinterpret_cast<int32_t*>(base + L.perm),
+                                            reinterpret_cast<int32_t*>(base + L.inv_perm), err, s));
+        if (st != KT_OK) return st;
     }
     {
         StageTimer timer(KT_STAGE_QUANT, s);
@@ -305,6 +318,23 @@ kt_status kt_mxfp4_moe_forward_ex(const uint16_t* hidden, int T, int H, const in
     }
     StageTimer timer(KT_STAGE_COMBINE, s);
     return cuda_status(launch_combine(y, topk_ids, T, H, k, E, out, s));
+}
+
+kt_status kt_mxfp4_moe_forward_ex(const uint16_t* hidden, int T, int H, const int32_t* topk_ids,
+                                  const float* topk_w, int k, const uint8_t* w13, const uint8_t* w13_sf,
+                                  const uint8_t* w2, const uint8_t* w2_sf, int E, int I, uint16_t* out, void* ws,
+                                  size_t ws_bytes, const kt_moe_options* opts, void* stream) {
+    return forward_impl(hidden, T, H, topk_ids, topk_w, k, false, nullptr, nullptr, nullptr, w13, w13_sf, w2, w2_sf,
+                        E, I, out, ws, ws_bytes, opts, stream);
+}
+
+kt_status kt_mxfp4_moe_forward_routed(const uint16_t* hidden, int T, int H, const int32_t* topk_ids,
+                                      const float* topk_w, int k, const int32_t* expert_offsets, const int32_t* perm,
+                                      const int32_t* inv_perm, const uint8_t* w13, const uint8_t* w13_sf,
+                                      const uint8_t* w2, const uint8_t* w2_sf, int E, int I, uint16_t* out, void* ws,
+                                      size_t ws_bytes, const kt_moe_options* opts, void* stream) {
+    return forward_impl(hidden, T, H, topk_ids, topk_w, k, true, expert_offsets, perm, inv_perm, w13, w13_sf, w2,
+                        w2_sf, E, I, out, ws, ws_bytes, opts, stream);
 }
 
 kt_status kt_mxfp4_moe_decode(const float* logits, const uint16_t* hidden, int T, int H, int E, int k, int I,

@@ -93,6 +93,27 @@ def test_forward_pointer_and_workspace_checks():
     assert "workspace" in kt.lib().kt_last_error().decode()
 
 
+def test_routed_forward_checks():
+    """kt_mxfp4_moe_forward_routed: the forward's checks, then its own routing arrays (null, alignment)."""
+    L = kt.lib()
+    v = lambda x: None if x is None else ctypes.c_void_p(x)
+
+    def fwd(off=P, perm=P, inv=P, T=4, H=256, I=256, E=8, k=2, hidden=P, ws_bytes=0):
+        return L.kt_mxfp4_moe_forward_routed(v(hidden), T, H, v(P), v(P), k, v(off), v(perm), v(inv), v(P), v(P),
+                                             v(P), v(P), E, I, v(P), v(P), ws_bytes, None, None)
+
+    assert fwd(T=-1) == INVALID
+    assert fwd(H=100) == SHAPE
+    assert fwd(T=0, off=None, perm=None, inv=None) == KT_OK
+    assert fwd(off=None) == INVALID
+    assert fwd(inv=None) == INVALID
+    assert "routing" in L.kt_last_error().decode()
+    assert fwd(hidden=None, off=None) == INVALID
+    assert fwd(perm=P + 4) == ALIGN
+    need = kt.workspace_bytes(4, 256, 256, 8, 2)
+    assert fwd(ws_bytes=need - 1) == WS
+
+
 def _route(T=4, E=8, k=2, logits=P, ids=P, w=P, off=P, perm=P, inv=P, ws=P, ws_bytes=0):
     v = lambda x: None if x is None else ctypes.c_void_p(x)
     return kt.lib().kt_moe_route_permute(v(logits), T, E, k, 1, v(ids), v(w), v(off), v(perm), v(inv), v(ws),

@@ -193,3 +193,30 @@ def test_forward_token_order_invariance():
                    torch.from_numpy(w[p]).cuda(), *W)
     torch.cuda.synchronize()
     assert torch.equal(a[torch.from_numpy(p).cuda()].view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("shape,opts", [
+    ((32, 1024, 16, 4, 512), {}),
+    ((600, 256, 4, 1, 128), {}),
+    ((400, 512, 3, 2, 640), {}),
+    ((25, 384, 2, 2, 640), dict(gate_up="interleaved", activation="swiglu_clamped", limit=0.5)),
+])
+def test_forward_on_a_given_routing_matches_forward(shape, opts):
+    """kt_mxfp4_moe_forward_routed reuses route_permute's permutation: bit-identical output, A1 and A2."""
+    T, H, E, k, I = shape
+    g = torch.Generator(device="cpu").manual_seed(T + H)
+    hidden = syn.make_hidden(T, H, seed=T, device="cuda")
+    logits = torch.randn(T, E, generator=g).cuda()
+    W = syn.make_weights(E, H, I, seed=3, device="cuda")
+    ids, w, offs, perm, inv = kt.route_permute(logits, k)
+    ws_a = torch.empty(kt.workspace_bytes(T, H, I, E, k), dtype=torch.uint8, device="cuda")
+    ws_b = torch.empty_like(ws_a)
+    out_a = kt.forward(hidden, ids, w, *W, workspace=ws_a, **opts)
+    out_b = kt.forward(hidden, ids, w, *W, workspace=ws_b, routing=(offs, perm, inv), **opts)
+    torch.cuda.synchronize()
+    assert kt.read_device_error(ws_a) == 0 and kt.read_device_error(ws_b) == 0
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    lay = kt.workspace_layout(T, H, I, E, k)
+    S = T * k
+    for name, nbytes in (("a1", S * H), ("a2", S * I)):
+        assert torch.equal(ws_a[lay[name]:lay[name] + nbytes], ws_b[lay[name]:lay[name] + nbytes]), name
