@@ -232,7 +232,9 @@ kt_status kt_mxfp4_moe_forward_ex(const uint16_t* hidden, int T, int H,
 
 /*
  * kt_mxfp4_moe_forward_ex on a routing that kt_moe_route_permute (or
- * kt_moe_route_permute_noalloc) has already permuted: expert_offsets [E+1],
+ * kt_moe_route_permute_noalloc) has already permuted (a convenience of this
+ * library; the pages route and run the layer as two steps, and this entry
+ * point only avoids redoing the first one's permutation): expert_offsets [E+1],
  * perm [S] and inv_perm [S] (S = T * k; device pointers, 16-byte aligned)
  * are that call's outputs for the same topk_ids and are used as they are,
  * so the forward skips its own histogram -> scan -> scatter (three launches;
