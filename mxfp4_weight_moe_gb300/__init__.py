@@ -24,7 +24,7 @@ from . import build_ext
 __all__ = [
     "KTError", "lib", "route_permute", "forward", "workspace_bytes", "workspace_layout", "read_device_error",
     "grouped_gemm_f32", "Layerwise", "status_string", "check_fc_shapes", "kernel_launches", "profile_enable",
-    "profile_read", "STAGES", "route_permute_noalloc", "decode", "DECODE_MAX_SLOTS",
+    "profile_read", "STAGES", "route_permute_noalloc", "decode", "DECODE_MAX_SLOTS", "MoeLayer",
 ]
 
 KT_OK = 0
@@ -409,6 +409,97 @@ def profile_read() -> dict:
     calls = (ctypes.c_int * len(STAGES))()
     _check(lib().kt_moe_profile_read(ms, calls), "kt_moe_profile_read")
     return {name: (float(ms[i]), int(calls[i])) for i, name in enumerate(STAGES)}
+
+
+class MoeLayer:
+    """One MoE layer whose packed experts are checked once, for repeated steps.
+
+    A call routes the step's logits and runs the layer: batches of at most
+    DECODE_MAX_SLOTS slots on a layer of at most 1 GiB of experts as one
+    decode launch (kt_mxfp4_moe_decode), others as kt_moe_route_permute +
+    kt_mxfp4_moe_forward_routed.  Per step only the step's own tensors are
+    checked and marshalled; workspaces and routing buffers are kept per T.
+    Results are those of route_permute + forward (or decode) with the same
+    options.  Returns (out, topk_ids, topk_w); the three are reused by the
+    next call with the same T unless `out` is given."""
+
+    _DECODE_MAX_LAYER_BYTES = 1 << 30
+
+    def __init__(self, w13: torch.Tensor, w13_sf: torch.Tensor, w2: torch.Tensor, w2_sf: torch.Tensor, k: int,
+                 renormalize: bool = True, gate_up: str = "halves", activation: str = "swiglu", alpha: float = 1.702,
+                 limit: float = 7.0):
+        dev = w13.device
+        for name, t in (("w13", w13), ("w13_sf", w13_sf), ("w2", w2), ("w2_sf", w2_sf)):
+            _need(t, name, torch.uint8, 3, dev)
+        E, I, H = check_fc_shapes(w13, w2)
+        if w13_sf.shape != (E, 2 * I, H // 32) or w2_sf.shape != (E, H, I // 32):
+            raise ValueError("scale tensors must be [E, 2I, H/32] and [E, H, I/32]")
+        if gate_up not in GATE_UP_LAYOUTS or activation not in ACTIVATIONS:
+            raise ValueError(f"gate_up must be one of {GATE_UP_LAYOUTS} and activation one of {ACTIVATIONS}")
+        self.E, self.I, self.H, self.k = E, I, H, int(k)
+        self.renormalize = int(bool(renormalize))
+        self.device = dev
+        self._dev_idx = w13.get_device()
+        self._weights = (w13, w13_sf, w2, w2_sf)   # keep them alive
+        self._wp = tuple(t.data_ptr() for t in self._weights)
+        self._opts = MoeOptions(GATE_UP_LAYOUTS.index(gate_up), ACTIVATIONS.index(activation), float(alpha),
+                                float(limit))
+        self._optsref = ctypes.byref(self._opts)
+        layer_bytes = sum(t.numel() for t in self._weights)
+        self._decode_ok = layer_bytes <= self._DECODE_MAX_LAYER_BYTES
+        self._per_T = {}
+
+    def _buffers(self, T: int):
+        b = self._per_T.get(T)
+        if b is None:
+            dev, E, k, H, I = self.device, self.E, self.k, self.H, self.I
+            decode = self._decode_ok and T * k <= DECODE_MAX_SLOTS
+            ws = torch.empty(max(workspace_bytes(T, H, I, E, k), 1), dtype=torch.uint8, device=dev)
+            route = (torch.empty(T, k, dtype=torch.int32, device=dev), torch.empty(T, k, dtype=torch.float32, device=dev),
+                     torch.empty(E + 1, dtype=torch.int32, device=dev), torch.empty(T * k, dtype=torch.int32, device=dev),
+                     torch.empty(T * k, dtype=torch.int32, device=dev))
+            rws = None if decode else torch.empty(max(int(lib().kt_moe_route_workspace_bytes(T, E, k)), 1),
+                                                  dtype=torch.uint8, device=dev)
+            out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+            b = (decode, ws, route, rws, out)
+            self._per_T[T] = b
+        return b
+
+    def __call__(self, hidden: torch.Tensor, logits: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+        T = hidden.shape[0]
+        if (hidden.dtype != torch.bfloat16 or logits.dtype != torch.float32 or hidden.shape != (T, self.H)
+                or logits.shape != (T, self.E) or hidden.get_device() != self._dev_idx
+                or logits.get_device() != self._dev_idx or not hidden.is_contiguous() or not logits.is_contiguous()):
+            raise ValueError(f"hidden must be contiguous bf16 [T, {self.H}] and logits contiguous f32 [T, {self.E}] "
+                             f"on {self.device}")
+        decode, ws, route, rws, own_out = self._buffers(T)
+        if out is None:
+            out = own_out
+        elif (out.dtype != torch.bfloat16 or out.shape != (T, self.H) or out.get_device() != self._dev_idx
+              or not out.is_contiguous()):
+            raise ValueError(f"out must be contiguous bf16 [T, {self.H}] on {self.device}")
+        ids, w, offs, perm, inv = route
+        with _on_device(self.device):
+            self._launch(T, hidden, logits, out, decode, ws, ids, w, offs, perm, inv, rws,
+                         _stream_ptr(stream, self.device))
+        return out, ids, w
+
+    def _launch(self, T, hidden, logits, out, decode, ws, ids, w, offs, perm, inv, rws, sp):
+        w13, w13_sf, w2, w2_sf = self._wp
+        L = lib()
+        if decode:
+            _check(L.kt_mxfp4_moe_decode(logits.data_ptr(), hidden.data_ptr(), T, self.H, self.E, self.k, self.I,
+                                         self.renormalize, w13, w13_sf, w2, w2_sf, ids.data_ptr(), w.data_ptr(),
+                                         out.data_ptr(), ws.data_ptr(), ws.numel(), self._optsref, sp),
+                   "kt_mxfp4_moe_decode")
+        else:
+            _check(L.kt_moe_route_permute(logits.data_ptr(), T, self.E, self.k, self.renormalize, ids.data_ptr(),
+                                          w.data_ptr(), offs.data_ptr(), perm.data_ptr(), inv.data_ptr(),
+                                          rws.data_ptr(), rws.numel(), sp), "kt_moe_route_permute")
+            _check(L.kt_mxfp4_moe_forward_routed(hidden.data_ptr(), T, self.H, ids.data_ptr(), w.data_ptr(), self.k,
+                                                 offs.data_ptr(), perm.data_ptr(), inv.data_ptr(), w13, w13_sf, w2,
+                                                 w2_sf, self.E, self.I, out.data_ptr(), ws.data_ptr(), ws.numel(),
+                                                 self._optsref, sp), "kt_mxfp4_moe_forward_routed")
 
 
 class Layerwise:

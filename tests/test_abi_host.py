@@ -199,6 +199,14 @@ def test_python_wrapper_checks_fc1_is_twice_fc2():
         kt.check_fc_shapes(torch.zeros(2, 128, 64, dtype=torch.uint8), w2)
 
 
+def test_moe_layer_rejects_cpu_weights():
+    E, H, I = 2, 128, 128
+    W = (torch.zeros(E, 2 * I, H // 2, dtype=torch.uint8), torch.zeros(E, 2 * I, H // 32, dtype=torch.uint8),
+         torch.zeros(E, H, I // 2, dtype=torch.uint8), torch.zeros(E, H, I // 32, dtype=torch.uint8))
+    with pytest.raises(ValueError):
+        kt.MoeLayer(*W, 2)
+
+
 def test_ops_reject_cpu_tensors():
     x = torch.zeros(2, 256, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):

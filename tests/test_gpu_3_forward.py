@@ -220,3 +220,25 @@ def test_forward_on_a_given_routing_matches_forward(shape, opts):
     S = T * k
     for name, nbytes in (("a1", S * H), ("a2", S * I)):
         assert torch.equal(ws_a[lay[name]:lay[name] + nbytes], ws_b[lay[name]:lay[name] + nbytes]), name
+
+
+@pytest.mark.parametrize("shape,opts", [
+    ((32, 1024, 16, 4, 512), {}),                                       # decode-sized: one launch
+    ((600, 256, 4, 1, 128), {}),                                        # routing + routed forward
+    ((25, 384, 2, 2, 640), dict(gate_up="interleaved", activation="swiglu_clamped", limit=0.5)),
+])
+def test_moe_layer_matches_route_and_forward(shape, opts):
+    """MoeLayer (experts checked once, buffers kept per T) gives the bits of route_permute + forward."""
+    T, H, E, k, I = shape
+    W = syn.make_weights(E, H, I, seed=5, device="cuda")
+    layer = kt.MoeLayer(*W, k, **opts)
+    for t in (T, max(1, T // 3), T):   # a second T, then the first again (kept buffers)
+        hidden = syn.make_hidden(t, H, seed=t, device="cuda")
+        g = torch.Generator(device="cpu").manual_seed(t)
+        logits = torch.randn(t, E, generator=g).cuda()
+        out, ids, w = layer(hidden, logits)
+        ids_r, w_r, *_ = kt.route_permute(logits, k)
+        ref = kt.forward(hidden, ids_r, w_r, *W, **opts)
+        torch.cuda.synchronize()
+        assert torch.equal(ids, ids_r) and torch.equal(w, w_r)
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), t
