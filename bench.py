@@ -373,13 +373,12 @@ def run_ours(args, cfg, full: bool = True):
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    # Decode-sized batches of small layers run as ONE launch (routing, permutation and the layer forward),
-    # where the separate launches' latency is most of the step.  Where the step streams gigabytes of experts
-    # (the Kimi-K3-shaped layer at T=16: 9 GB) launch latency is noise, and the separate GEMM launches
-    # measured faster than the single launch's GEMM passes; auto keeps those on the multi-launch path.
-    layer_weight_bytes = E * (2 * I * H // 2 + 2 * I * H // 32 + H * I // 2 + H * I // 32)
-    use_decode = args.path == "decode" or (args.path == "auto" and T * k <= kt.DECODE_MAX_SLOTS
-                                           and layer_weight_bytes <= (1 << 30))
+    # auto runs the separate launches (routing, then the forward on its permutation).  The single-launch
+    # decode kernel is there with --path decode: measured on GB300 with every step starting from DRAM (the
+    # L2 flush below), the separate launches were 0-8 us faster on the tiny and small layers and 10-17 us
+    # faster replayed in a CUDA graph; on the 9 GB Kimi-shaped T=16 layer the separate GEMM launches are
+    # faster too.
+    use_decode = args.path == "decode"
 
     def step(h=hidden, lg=logits, o=out, s=stream):
         if use_decode:
@@ -674,8 +673,8 @@ def main():
                                                           "under 'secondary' ('none' to skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", choices=("auto", "decode", "multi"), default="auto",
-                    help="auto: the single-launch decode kernel when T * top_k <= 2048 and the layer's experts "
-                         "hold at most 1 GiB, else route_permute + forward")
+                    help="decode: the single-launch decode kernel (T * top_k <= 2048); auto and multi: "
+                         "route_permute + forward_routed")
     ap.add_argument("--ref-budget-s", type=float, default=150.0)
     ap.add_argument("--layer-stores", type=int, default=4,
                     help="layerwise workload: distinct pinned host layer stores, cycled over the layers")

@@ -414,20 +414,18 @@ def profile_read() -> dict:
 class MoeLayer:
     """One MoE layer whose packed experts are checked once, for repeated steps.
 
-    A call routes the step's logits and runs the layer: batches of at most
-    DECODE_MAX_SLOTS slots on a layer of at most 1 GiB of experts as one
-    decode launch (kt_mxfp4_moe_decode), others as kt_moe_route_permute +
-    kt_mxfp4_moe_forward_routed.  Per step only the step's own tensors are
+    A call routes the step's logits and runs the layer as kt_moe_route_permute
+    + kt_mxfp4_moe_forward_routed, or (single_launch=True, for batches of at
+    most DECODE_MAX_SLOTS slots) as one kt_mxfp4_moe_decode launch.  Per step
+    only the step's own tensors are
     checked and marshalled; workspaces and routing buffers are kept per T.
     Results are those of route_permute + forward (or decode) with the same
     options.  Returns (out, topk_ids, topk_w); the three are reused by the
     next call with the same T unless `out` is given."""
 
-    _DECODE_MAX_LAYER_BYTES = 1 << 30
-
     def __init__(self, w13: torch.Tensor, w13_sf: torch.Tensor, w2: torch.Tensor, w2_sf: torch.Tensor, k: int,
                  renormalize: bool = True, gate_up: str = "halves", activation: str = "swiglu", alpha: float = 1.702,
-                 limit: float = 7.0):
+                 limit: float = 7.0, single_launch: bool = False):
         dev = w13.device
         for name, t in (("w13", w13), ("w13_sf", w13_sf), ("w2", w2), ("w2_sf", w2_sf)):
             _need(t, name, torch.uint8, 3, dev)
@@ -445,15 +443,14 @@ class MoeLayer:
         self._opts = MoeOptions(GATE_UP_LAYOUTS.index(gate_up), ACTIVATIONS.index(activation), float(alpha),
                                 float(limit))
         self._optsref = ctypes.byref(self._opts)
-        layer_bytes = sum(t.numel() for t in self._weights)
-        self._decode_ok = layer_bytes <= self._DECODE_MAX_LAYER_BYTES
+        self._single_launch = bool(single_launch)
         self._per_T = {}
 
     def _buffers(self, T: int):
         b = self._per_T.get(T)
         if b is None:
             dev, E, k, H, I = self.device, self.E, self.k, self.H, self.I
-            decode = self._decode_ok and T * k <= DECODE_MAX_SLOTS
+            decode = self._single_launch and T * k <= DECODE_MAX_SLOTS
             ws = torch.empty(max(workspace_bytes(T, H, I, E, k), 1), dtype=torch.uint8, device=dev)
             route = (torch.empty(T, k, dtype=torch.int32, device=dev), torch.empty(T, k, dtype=torch.float32, device=dev),
                      torch.empty(E + 1, dtype=torch.int32, device=dev), torch.empty(T * k, dtype=torch.int32, device=dev),

@@ -222,16 +222,17 @@ def test_forward_on_a_given_routing_matches_forward(shape, opts):
         assert torch.equal(ws_a[lay[name]:lay[name] + nbytes], ws_b[lay[name]:lay[name] + nbytes]), name
 
 
-@pytest.mark.parametrize("shape,opts", [
-    ((32, 1024, 16, 4, 512), {}),                                       # decode-sized: one launch
-    ((600, 256, 4, 1, 128), {}),                                        # routing + routed forward
-    ((25, 384, 2, 2, 640), dict(gate_up="interleaved", activation="swiglu_clamped", limit=0.5)),
+@pytest.mark.parametrize("shape,opts,single", [
+    ((32, 1024, 16, 4, 512), {}, True),                                 # decode-sized, one launch
+    ((32, 1024, 16, 4, 512), {}, False),                                # decode-sized, routing + routed forward
+    ((600, 256, 4, 1, 128), {}, False),
+    ((25, 384, 2, 2, 640), dict(gate_up="interleaved", activation="swiglu_clamped", limit=0.5), True),
 ])
-def test_moe_layer_matches_route_and_forward(shape, opts):
+def test_moe_layer_matches_route_and_forward(shape, opts, single):
     """MoeLayer (experts checked once, buffers kept per T) gives the bits of route_permute + forward."""
     T, H, E, k, I = shape
     W = syn.make_weights(E, H, I, seed=5, device="cuda")
-    layer = kt.MoeLayer(*W, k, **opts)
+    layer = kt.MoeLayer(*W, k, single_launch=single, **opts)
     for t in (T, max(1, T // 3), T):   # a second T, then the first again (kept buffers)
         hidden = syn.make_hidden(t, H, seed=t, device="cuda")
         g = torch.Generator(device="cpu").manual_seed(t)
