@@ -251,20 +251,19 @@ static kt_status forward_impl(const uint16_t* hidden, int T, int H, const int32_
     const long long S = static_cast<long long>(T) * k;
 
     if ((st = cuda_status(cudaMemsetAsync(err, 0, sizeof(int), s))) != KT_OK) return st;
-    {
+    if (!routed) {
         StageTimer timer(KT_STAGE_PERMUTE, s);
-        if (routed)
-            st = cuda_status(launch_chunk_prefix(offsets, E, chunk_prefix, s));
-        else
-            st = cuda_status(launch_permute(topk_ids, S, E, reinterpret_cast<int32_t*>(base + L.hist),
-                                            reinterpret_cast<int32_t*>(base + L.expert_offsets), chunk_prefix,
-                                            reinterpret_cast<int32_t*>(base + L.perm),
-                                            reinterpret_cast<int32_t*>(base + L.inv_perm), err, s));
-        if (st != KT_OK) return st;
+        if ((st = cuda_status(launch_permute(topk_ids, S, E, reinterpret_cast<int32_t*>(base + L.hist),
+                                             reinterpret_cast<int32_t*>(base + L.expert_offsets), chunk_prefix,
+                                             reinterpret_cast<int32_t*>(base + L.perm),
+                                             reinterpret_cast<int32_t*>(base + L.inv_perm), err, s))) != KT_OK)
+            return st;
     }
     {
+        // on a given routing, the quantiser's launch also derives the per-expert chunk counts
         StageTimer timer(KT_STAGE_QUANT, s);
-        if ((st = cuda_status(launch_quant_scatter(hidden, T, H, k, inv_perm, a1, a1_sf, sf_rows(S), s))) != KT_OK)
+        if ((st = cuda_status(launch_quant_scatter(hidden, T, H, k, inv_perm, a1, a1_sf, sf_rows(S), s,
+                                                   routed ? offsets : nullptr, E, chunk_prefix))) != KT_OK)
             return st;
     }
 

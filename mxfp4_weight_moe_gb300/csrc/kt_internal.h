@@ -79,9 +79,11 @@ cudaError_t launch_permute(const int32_t* ids, long long S, int E, int32_t* hist
 // chunk_prefix [E+1] from expert_offsets alone (for the diagnostic GEMM).
 cudaError_t launch_chunk_prefix(const int32_t* expert_offsets, int E, int32_t* chunk_prefix, cudaStream_t s);
 // MXFP8 quantisation of hidden rows, each written to its k permuted rows
-// (codes [S, H]; scales K-step-major with S4 = sf_rows(S)).
+// (codes [S, H]; scales K-step-major with S4 = sf_rows(S)).  With `offsets`
+// (expert_offsets [E+1]) the same launch also writes chunk_prefix [E+1].
 cudaError_t launch_quant_scatter(const uint16_t* hidden, int T, int H, int k, const int32_t* inv_perm, uint8_t* a1,
-                                 uint8_t* a1_sf, int S4, cudaStream_t s);
+                                 uint8_t* a1_sf, int S4, cudaStream_t s, const int32_t* offsets = nullptr, int E = 0,
+                                 int32_t* chunk_prefix = nullptr);
 // Plain [S, K/32] scale bytes -> K-step-major layout (diagnostic GEMM entry).
 cudaError_t launch_sf_to_kstep_major(const uint8_t* plain, int S, int K, uint8_t* out, int S4, cudaStream_t s);
 // out[t] = sum over valid slots of y[t*k + j] (y already weighted).

@@ -7,18 +7,47 @@
 // rule floor(log2 amax) - 8 and elements are converted with round-to-
 // nearest-even, saturating at +-448.
 #include "kt_common.cuh"
+#include "kt_decode_dev.cuh"
 #include "kt_internal.h"
 #include "kt_quant_dev.cuh"
 
 namespace kt {
 
 // One warp per (token row, pass of 1024 elements) (quant_token_warp in kt_quant_dev.cuh).
+// With `offsets` given, one extra block (the last) also derives chunk_prefix
+// [E+1] from expert_offsets [E+1]: the chunks of kChunkRows rows each expert's
+// rows split into, as an exclusive prefix sum (what the permutation kernels
+// write), for a forward that reuses a routing call's permutation.
 __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __restrict__ hidden, int T, int H, int k,
                                                             const int32_t* __restrict__ inv_perm,
                                                             uint8_t* __restrict__ a1, uint8_t* __restrict__ a1_sf,
-                                                            int S4) {
+                                                            int S4, const int32_t* __restrict__ offsets, int E,
+                                                            int32_t* __restrict__ chunk_prefix) {
     griddep_wait();
     griddep_launch_dependents();
+    if (offsets != nullptr && blockIdx.x == gridDim.x - 1) {
+        __shared__ int s_warp[33];
+        constexpr int kPer = (kMaxExperts + 255) / 256;   // experts per thread
+        int nch[kPer];
+        int mine = 0;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int e = static_cast<int>(threadIdx.x) * kPer + u;
+            const int cnt = e < E ? offsets[e + 1] - offsets[e] : 0;
+            nch[u] = cnt > 0 ? (cnt + kChunkRows - 1) / kChunkRows : 0;
+            mine += nch[u];
+        }
+        int total;
+        int run = block_exclusive_scan(mine, s_warp, &total);
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int e = static_cast<int>(threadIdx.x) * kPer + u;
+            if (e < E) chunk_prefix[e] = run;
+            run += nch[u];
+        }
+        if (threadIdx.x == 0) chunk_prefix[E] = total;
+        return;
+    }
     __shared__ int s_dst[8][kMaxTopK];
     const int wib = threadIdx.x >> 5;
     const int per_row = quant_items_per_row(H);
@@ -30,11 +59,13 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint16_t* __re
 }
 
 cudaError_t launch_quant_scatter(const uint16_t* hidden, int T, int H, int k, const int32_t* inv_perm, uint8_t* a1,
-                                 uint8_t* a1_sf, int S4, cudaStream_t s) {
+                                 uint8_t* a1_sf, int S4, cudaStream_t s, const int32_t* offsets, int E,
+                                 int32_t* chunk_prefix) {
     if (T <= 0) return cudaSuccess;
     const long long items = static_cast<long long>(T) * quant_items_per_row(H);
-    const cudaError_t e = launch_chained(quant_scatter_kernel, dim3(static_cast<unsigned>((items + 7) / 8)), dim3(256),
-                                         0, s, hidden, T, H, k, inv_perm, a1, a1_sf, S4);
+    const unsigned blocks = static_cast<unsigned>((items + 7) / 8) + (offsets != nullptr ? 1u : 0u);
+    const cudaError_t e = launch_chained(quant_scatter_kernel, dim3(blocks), dim3(256), 0, s, hidden, T, H, k, inv_perm,
+                                         a1, a1_sf, S4, offsets, E, chunk_prefix);
     count_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
