@@ -136,8 +136,7 @@ kt_status kt_moe_route_permute(const float* logits, int T, int E, int k, int ren
  *   - Every call looks up the array's device address in the current
  *     device's context (cudaGetSymbolAddress, a host-side lookup), so the
  *     address stays right after a context reset.  The first call on a
- *     device may also load the library's device code into that context;
- *     make that first call before any stream capture on the device.
+ *     device may also load the library's device code into that context.
  *   - All calls share the one array and leave their scratch in it; each call
  *     clears the error word it uses and fully rewrites the rest before
  *     reading it.  Calls that overlap on the GPU (other streams, other host
