@@ -1458,9 +1458,8 @@ static bool encode_maps(const GemmArgs& a, GemmMaps& maps) {
     const bool sfa_tma = (a.K % 512) == 0;
     bool ok = true;
     const bool inter = fc1 && a.interleaved;
-    // Weight tiles: with the A operand in tensor memory, packed bytes (64 per row per K quad) in the 64-byte
-    // swizzle the expanding warps read conflict-free; otherwise the unpacking type (one byte per element) in
-    // the 128-byte swizzle the MMA reads.  x counts bytes or elements accordingly.
+    // Weight tiles: the unpacking type (one byte per element in shared memory, 64 packed bytes per row per
+    // K quad read) in the 128-byte swizzle the MMA reads; x counts elements.
     const CUtensorMapDataType wt = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
     const uint64_t wx = 128;
     const CUtensorMapSwizzle wsw = CU_TENSOR_MAP_SWIZZLE_128B;
