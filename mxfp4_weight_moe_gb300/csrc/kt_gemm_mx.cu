@@ -111,7 +111,8 @@ constexpr uint32_t kAccCols = kTileTokens;    // accumulator buffer b at column 
 constexpr uint32_t kTmemSF = 2 * kAccCols;    // scale columns after both accumulators
 constexpr uint32_t kSfQuadCols = 12;          // per K quad: 4 weight + 8 token scale columns
 constexpr uint32_t kSfGroupCols = kGroup * kSfQuadCols;   // one scale group's tensor-memory buffer (two of them)
-constexpr int kPrefetchGroups = 2;            // scale-warp L2 prefetch distance, in groups
+constexpr int kPrefetchGroups = 2;            // scale-warp L2 prefetch distance, in groups (decode-sized launches)
+constexpr int kPrefetchNearRows = 64;         // launches with this many token rows per expert prefetch at distance 0
 // the largest stage always fits once every earlier stage is released
 static_assert(2 * kQuadW + kSmallN * 256 <= kRing && kQuadW + kTileTokens * 128 <= kRing, "stage ring");
 static_assert(kSmemTotal <= 232448, "shared memory budget");
@@ -159,6 +160,7 @@ struct KParams {
     int interleaved;          // FC1: w13 rows interleave gate / up (row 2i gate i, row 2i+1 up i)
     int act;                  // FC1: 0 SwiGLU, 1 clamped SwiGLU
     float alpha, limit;       // clamped SwiGLU parameters
+    int pf_near;              // 1: each group's weights are prefetched into L2 as its scales are built
 };
 
 // The routing tables a CTA decodes its work units from.  chunk_prefix is
@@ -614,7 +616,7 @@ __device__ __forceinline__ bool wait_count(unsigned* ctr, unsigned target, volat
 // GEMM; NP = 2 with MODE kFused: FC1 then FC2 of the decode kernel, whose
 // prologue and combine phases also run here, d != nullptr).  M[i] and PP[i]
 // live in kernel parameter space.
-template <int MODE, int NP>
+template <int MODE, int NP, bool NEAR>
 __device__ __forceinline__ void gemm_body(const GemmMaps* M, const KParams* PP, const DecodeArgs* d) {
     const KParams& p = PP[0];   // fields every pass shares (E, cl, tables, error word, wait limits)
     extern __shared__ uint8_t smem_raw[];
@@ -921,14 +923,22 @@ __device__ __forceinline__ void gemm_body(const GemmMaps* M, const KParams* PP, 
                 tma_load_2d(dst + kStgSFA, &mm.asf, stg_bar(buf), c.ti.r_al, c.g * kGroup);
             }
         };
+        // L2 prefetch of a group's packed weight bytes: whole 128-byte lines, four K quads of each row at
+        // once, where the stage boxes later read one or two quads of each row.  Prefill-sized launches
+        // (NEAR) prefetch each group as its scales are built, which measured faster than any distance
+        // ahead; decode-sized launches (2-quad stages, a few rows per tile) kPrefetchGroups of this warp's
+        // groups ahead.
+        constexpr bool pf_near = NEAR;
         auto prefetch_group = [&](const GroupCursor<MODE, NP>& c) {
             if (lane == 0 && c.valid)
                 prefetch_weight_box(P[c.pass].fc1, &P[c.pass].m->wpf, c.g * (kGroup * 128 / 2), c.wy, c.wz,
                                     P[c.pass].p->interleaved != 0);
         };
-        for (int i = 0; i < kPrefetchGroups; ++i) {   // this warp's next groups
-            prefetch_group(pf);
-            advance2(pf);
+        if (!pf_near) {
+            for (int i = 0; i < kPrefetchGroups; ++i) {   // this warp's next groups
+                prefetch_group(pf);
+                advance2(pf);
+            }
         }
         issue_staging(ahead, 2 * sw);   // staging for this warp's first group
         advance2(ahead);
@@ -950,8 +960,12 @@ __device__ __forceinline__ void gemm_body(const GemmMaps* M, const KParams* PP, 
             }
             issue_staging(ahead, 2 * sw + ((lidx + 1) & 1));
             advance2(ahead);
-            prefetch_group(pf);
-            advance2(pf);
+            if (pf_near) {
+                prefetch_group(cur);
+            } else {
+                prefetch_group(pf);
+                advance2(pf);
+            }
             ok = __all_sync(0xffffffffu, mbar_wait(stg_bar(sbuf), (stg_ph >> sbuf) & 1u, abort_flag,
                                                    p.wait_limit_ns));
             if (!ok) break;
@@ -1313,10 +1327,11 @@ __device__ __forceinline__ void gemm_body(const GemmMaps* M, const KParams* PP, 
     }
 }
 
-template <int MODE>
+// NEAR: the L2 weight prefetch of prefill-sized launches (see the scale warps)
+template <int MODE, bool NEAR>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ KParams p) {
-    gemm_body<MODE, 1>(&maps, &p, nullptr);
+    gemm_body<MODE, 1, NEAR>(&maps, &p, nullptr);
 }
 
 // The single-launch decode kernel: routing, permutation, quantisation, FC1,
@@ -1328,7 +1343,7 @@ struct DecodeParams {
 };
 
 __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_constant__ DecodeParams dp) {
-    gemm_body<kFused, 2>(dp.maps, dp.p, &dp.d);
+    gemm_body<kFused, 2, false>(dp.maps, dp.p, &dp.d);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1391,7 +1406,7 @@ static int pick_cluster(int want, int* grid) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int nclusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&nclusters, mx_gemm_kernel<MODE>, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&nclusters, mx_gemm_kernel<MODE, false>, &cfg) != cudaSuccess) {
             cudaGetLastError();
             continue;
         }
@@ -1415,8 +1430,11 @@ static cudaError_t launch_mode(const GemmMaps& maps, KParams kp, int max_cluster
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<MODE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemTotal);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(mx_gemm_kernel<MODE, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmemTotal);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
@@ -1443,7 +1461,8 @@ static cudaError_t launch_mode(const GemmMaps& maps, KParams kp, int max_cluster
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = c > 1 ? 2 : 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, mx_gemm_kernel<MODE>, maps, kp);
+    cudaError_t e = kp.pf_near ? cudaLaunchKernelEx(&cfg, mx_gemm_kernel<MODE, true>, maps, kp)
+                               : cudaLaunchKernelEx(&cfg, mx_gemm_kernel<MODE, false>, maps, kp);
     count_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -1642,6 +1661,7 @@ static void fill_params(const GemmArgs& a, KParams& kp) {
     kp.wait_limit_ns = dbg.wait_limit_ns;
     kp.debug_flags = dbg.flags;
     kp.interleaved = inter ? 1 : 0;
+    kp.pf_near = static_cast<long long>(a.S) >= static_cast<long long>(kPrefetchNearRows) * a.E ? 1 : 0;
     kp.act = fc1 ? a.activation : 0;
     kp.alpha = a.alpha;
     kp.limit = a.limit;

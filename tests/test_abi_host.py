@@ -262,7 +262,7 @@ def test_chained_kernels_wait_before_touching_memory():
     bodies = _kernel_bodies(src)
     assert chained <= set(bodies), chained - set(bodies)
     # the GEMM kernels delegate to gemm_body (shared with the single-launch decode kernel)
-    assert "gemm_body<MODE, 1>" in bodies["mx_gemm_kernel"]
+    assert "gemm_body<MODE, 1, NEAR>" in bodies["mx_gemm_kernel"]
     m = re.search(r"void\s+gemm_body\s*\(", src)
     start = src.index("{", m.end())
     depth, i = 0, start
