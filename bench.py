@@ -61,11 +61,8 @@ FP8_OVER_BF16 = 2.0     # nominal dense ratio (4.5 / 2.25 PFLOP/s); mxf8f6f4 run
 # traffic null.
 GEMM_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mxfp4_weight_moe_gb300", "csrc", "kt_gemm_mx.cu")
 FC1_TRAFFIC = {
-    ("dsv4", "802e24481ce9e8648fbedcc657186c9d7e68dba60ee44dc9605cce4a4c0edd53"): 2460472064 + 52114688,
-    ("kimi_T8192", "802e24481ce9e8648fbedcc657186c9d7e68dba60ee44dc9605cce4a4c0edd53"): 28962077440 + 486142720,
-    # the same kernel: this source differs from the one above only in a comment of the host-side map code
-    ("dsv4", "91b78280d7c429938e2f072ba194bb08392f14cf820ae44f05ad83aa393b0053"): 2460472064 + 52114688,
-    ("kimi_T8192", "91b78280d7c429938e2f072ba194bb08392f14cf820ae44f05ad83aa393b0053"): 28962077440 + 486142720,
+    ("dsv4", "fd79b72d69a1d01a24bf2389aa0c7423ce2fb39c693b30cf8ab916b6e1eae91a"): 2386266368 + 52687872,
+    ("kimi_T8192", "fd79b72d69a1d01a24bf2389aa0c7423ce2fb39c693b30cf8ab916b6e1eae91a"): 25473608448 + 485629696,
 }
 
 
