@@ -63,6 +63,10 @@ GEMM_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mxfp4_weigh
 FC1_TRAFFIC = {
     ("dsv4", "fd79b72d69a1d01a24bf2389aa0c7423ce2fb39c693b30cf8ab916b6e1eae91a"): 2386266368 + 52687872,
     ("kimi_T8192", "fd79b72d69a1d01a24bf2389aa0c7423ce2fb39c693b30cf8ab916b6e1eae91a"): 25473608448 + 485629696,
+    ("kimi_T16", "fd79b72d69a1d01a24bf2389aa0c7423ce2fb39c693b30cf8ab916b6e1eae91a"): 6206675456 + 4165632,
+    ("small_T32", "fd79b72d69a1d01a24bf2389aa0c7423ce2fb39c693b30cf8ab916b6e1eae91a"): 8587776,
+    ("small_T1", "fd79b72d69a1d01a24bf2389aa0c7423ce2fb39c693b30cf8ab916b6e1eae91a"): 2334976,
+    ("tiny", "fd79b72d69a1d01a24bf2389aa0c7423ce2fb39c693b30cf8ab916b6e1eae91a"): 132864,
 }
 
 
